@@ -1,0 +1,31 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: large workload (full-size shapes)")
+
+
+def read_golden(name):
+    """Parse a whitespace table under tests/golden/: key -> (values, tol)."""
+    out = {}
+    with open(os.path.join(ROOT, "tests", "golden", name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            out[parts[0]] = ([float(x) for x in parts[1:-1]], float(parts[-1]))
+    return out
+
+
+@pytest.fixture
+def golden():
+    return read_golden
