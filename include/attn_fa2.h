@@ -1,0 +1,114 @@
+/*
+ * attn_fa2.h -- C ABI of the GB300 (sm_103a) FlashAttention-2-style fused
+ * attention forward library (libattn_fa2.so).
+ *
+ * The operation (per batch b, head h, query row i):
+ *     s_ij = scale * sum_c q[i,c] k[j,c]     for every key j (j <= i if causal)
+ *     O[i,:] = sum_j exp(s_ij - m_i) v[j,:] / l_i,   m_i = max_j s_ij,
+ *     l_i = sum_j exp(s_ij - m_i),   L[i] = m_i + ln l_i   (natural log)
+ * Defined by "Kernels and Memory in LLM Inference" (section "Attention, said
+ * plainly again": scores, row softmax with the max subtracted, weighted sum of
+ * V) and "FlashAttention-2 from PyTorch to Triton" (the FA2 forward pass: the
+ * N x N scores never leave the chip; L is the per-row logsumexp kept for the
+ * backward pass; causal keeps key j iff j <= query i).  FP8 inputs carry one
+ * descale per tensor, folded into the score scale and the output as in
+ * "1.8x Faster Attention on an RTX 5080: an FP8 Flash Attention Kernel in
+ * CuTe-DSL" (section "Who am I, what's mine?").
+ *
+ * Conventions for every entry point:
+ *   - Layout: q, k, v, o are [B, H, N, d] row-major and contiguous (d is the
+ *     fastest axis; heads of one batch entry follow each other); lse is
+ *     [B, H, N] fp32.  Queries and keys have the same length N.
+ *   - Ownership: the caller allocates and owns every buffer; the library
+ *     allocates no memory and keeps no pointer after the call returns.
+ *   - Execution: device entry points only enqueue work on `stream` (a
+ *     cudaStream_t passed as void*, NULL = the legacy default stream) and
+ *     return without synchronising.  The device pointers must stay valid until
+ *     the stream reaches the work.
+ *   - Errors: arguments are validated before anything is enqueued; on an
+ *     invalid argument nothing is launched and a non-zero attn_status_t is
+ *     returned; attn_last_error() gives a one-line message (per thread).
+ *     Device-side timeouts (a wait that exceeded the limit set by
+ *     attn_set_wait_limit_ns) are reported by attn_get_device_status().
+ */
+#ifndef ATTN_FA2_H
+#define ATTN_FA2_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v.  O is fp32 for ATTN_F32 and bf16 otherwise. */
+typedef enum {
+  ATTN_F32 = 0,  /* IEEE binary32; d in {16, 32, 64, 128}; CUDA-core kernel           */
+  ATTN_BF16 = 1, /* bfloat16; d in {64, 128}; tcgen05 tensor-core kernel             */
+  ATTN_E4M3 = 2  /* FP8 E4M3 (finite, max 448) codes; d = 128; tcgen05 tensor cores  */
+} attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, size < 1, non-finite or non-positive scale, bad flag */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for (e.g. d = 96 for bf16)  */
+  ATTN_ERR_MISALIGNED = 3,  /* q/k/v/o not 16-byte aligned, or lse not 4-byte aligned             */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; see attn_last_error()            */
+  ATTN_ERR_TIMEOUT = 5      /* a device-side wait exceeded its limit (attn_get_device_status)      */
+} attn_status_t;
+
+/*
+ * Attention forward on device buffers.
+ *   q, k, v : device, [B,H,N,d] of `dtype` (ATTN_E4M3: raw codes, descales 1).
+ *   o       : device, [B,H,N,d]; fp32 if dtype == ATTN_F32, else bf16.
+ *   lse     : device, [B,H,N] fp32, natural-log logsumexp of the scaled scores.
+ *   scale   : softmax scale (finite, > 0; 1/sqrt(d) is the usual value).
+ *   causal  : 0 = every key; 1 = key j kept iff j <= query i.
+ * Returns ATTN_OK once the kernel is enqueued on `stream`.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, int causal, int dtype, void* stream);
+
+/*
+ * FP8 E4M3 forward with per-tensor descales: the real value of a code c of q
+ * is e4m3(c) * q_descale (likewise k, v).  O is bf16, lse fp32.  Descales must
+ * be finite and > 0.  Other arguments as attn_fwd.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, float q_descale, float k_descale, float v_descale, int causal, void* stream);
+
+/*
+ * End-to-end forward from host buffers, for callers whose data lives in host
+ * memory: enqueues on `stream` the copies h_q/h_k/h_v -> d_q/d_k/d_v, the
+ * forward (as attn_fwd_fp8 for ATTN_E4M3, attn_fwd otherwise; descales are
+ * ignored unless dtype == ATTN_E4M3), then the copies d_o -> h_o and
+ * d_lse -> h_lse.  The caller provides both the host buffers (page-locked for
+ * the copies to be asynchronous) and the device buffers, and synchronises the
+ * stream before reading h_o / h_lse.  One cudaMemcpyAsync per buffer.
+ */
+int attn_fwd_host(const void* h_q, const void* h_k, const void* h_v, void* h_o, float* h_lse, void* d_q,
+                  void* d_k, void* d_v, void* d_o, float* d_lse, int B, int H, int N, int d, float scale,
+                  float q_descale, float k_descale, float v_descale, int causal, int dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait
+ * since the last call (its outputs are then undefined), or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int attn_get_device_status(void* stream);
+
+/* Upper bound (nanoseconds, >= 1e6) on any single device-side wait of later
+ * launches from this process; default 2e9 (2 s).  Returns the previous value. */
+uint64_t attn_set_wait_limit_ns(uint64_t ns);
+
+/* Static description of a status code. */
+const char* attn_status_string(int status);
+
+/* Message of the last failed call made by this thread ("" if none). */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FA2_H */

@@ -29,3 +29,12 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def built_library():
+    """Build libattn_fa2.so if it is missing or stale (nvcc cross-compiles for
+    sm_103a without a GPU) and return its path."""
+    from tiled_attention_fa2_gb300 import _build
+
+    return _build.build()

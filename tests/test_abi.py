@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/attn_fa2.h declares, and rejects invalid arguments
+before anything reaches CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_fa2_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_fa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib(built_library):
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_fp8", "attn_fwd_host", "attn_get_device_status",
+            "attn_status_string", "attn_last_error", "attn_set_wait_limit_ns"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.attn_status_string(0) == b"ok"
+    assert lib.attn_status_string(5) == b"device wait timed out"
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced on these paths
+
+
+def call_fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=256, d=64, scale=0.125, causal=0, dtype=1,
+             stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"], a["scale"],
+                        a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
+    (dict(causal=2), 1), (dict(dtype=7), 1),
+    (dict(d=96), 2), (dict(d=32), 2), (dict(dtype=2, d=64), 2), (dict(dtype=0, d=48), 2),
+    (dict(q=FAKE + 8), 3), (dict(o=FAKE + 4), 3), (dict(lse=FAKE + 2), 3),
+    (dict(B=65536, H=65536), 1),
+])
+def test_invalid_arguments_are_rejected_on_the_host(lib, kw, status):
+    assert call_fwd(lib, **kw) == status
+    assert lib.attn_last_error() != b""
+
+
+def test_fp8_descales_are_validated(lib):
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        st = lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 0.1, bad, 1.0, 1.0, 0, None)
+        assert st == 1
+
+
+def test_host_entry_validates_before_copying(lib):
+    st = lib.attn_fwd_host(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                           1, 1, 128, 64, 0.1, 1.0, 1.0, 1.0, 0, 1, None)
+    assert st == 1
+    st = lib.attn_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                           1, 1, 128, 64, 0.1, 1.0, 1.0, 1.0, 0, 9, None)
+    assert st == 1
+
+
+def test_wait_limit_setter_round_trips(lib):
+    old = lib.attn_set_wait_limit_ns(5_000_000_000)
+    assert lib.attn_set_wait_limit_ns(old) == 5_000_000_000
+    assert lib.attn_set_wait_limit_ns(10) == old
+    assert lib.attn_set_wait_limit_ns(old) == 1_000_000  # clamped to >= 1 ms
+
+
+def test_binding_raises_when_library_is_missing(tmp_path, monkeypatch):
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(ImportError):
+        binding.load_library(str(tmp_path / "missing.so"))

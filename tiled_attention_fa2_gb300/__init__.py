@@ -13,7 +13,8 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "forward", "inputs"]
 
 def __getattr__(name):
     if name in ("attn_fwd", "attn_fwd_fp8", "forward", "binding"):
-        from . import binding
+        import importlib
 
+        binding = importlib.import_module(__name__ + ".binding")
         return binding if name == "binding" else getattr(binding, name)
     raise AttributeError(name)

@@ -1,0 +1,173 @@
+"""ctypes binding of libattn_fa2.so (declared in include/attn_fa2.h).
+
+Argument marshalling only: torch tensors provide device memory and the CUDA
+stream; every step of the attention forward runs in the library's kernels.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libattn_fa2.so")
+
+ATTN_F32, ATTN_BF16, ATTN_E4M3 = 0, 1, 2
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
+                4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+
+# Every symbol include/attn_fa2.h declares, with its ctypes signature.
+_VP, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
+SIGNATURES = {
+    "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
+    "attn_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _VP]),
+    "attn_fwd_host": (_I, [_VP] * 10 + [_I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _VP]),
+    "attn_get_device_status": (_I, [_VP]),
+    "attn_set_wait_limit_ns": (_U64, [_U64]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_last_error": (ctypes.c_char_p, []),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} not found: build it with `python -m tiled_attention_fa2_gb300._build` "
+                              "(or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        raise AttnError(status, lib.attn_last_error().decode() or lib.attn_status_string(status).decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return ATTN_E4M3
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _shape(q, k, v):
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"q, k, v must share one [B, H, N, d] shape (got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)})")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must have the same dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _outputs(q, o, lse, B, H, N, d, code):
+    odt = torch.float32 if code == ATTN_F32 else torch.bfloat16
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if o.dtype != odt or tuple(o.shape) != (B, H, N, d) or not o.is_contiguous():
+        raise ValueError(f"o must be a contiguous {odt} tensor of shape {(B, H, N, d)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(B, H, N)}")
+    return o, lse
+
+
+def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """Attention forward on CUDA tensors [B, H, N, d] (float32, bfloat16, or
+    e4m3 codes with unit descales).  Returns (o, lse)."""
+    B, H, N, d = _shape(q, k, v)
+    code = _dtype_code(q)
+    o, lse = _outputs(q, o, lse, B, H, N, d, code)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    lib = load_library()
+    _check(lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                        scale, int(bool(causal)), code, _stream_handle(stream, q.device)))
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None, causal=False,
+                 stream=None):
+    """FP8 E4M3 forward (uint8 or float8_e4m3fn CUDA tensors) with per-tensor
+    descales; bf16 O, fp32 L.  Returns (o, lse)."""
+    B, H, N, d = _shape(q, k, v)
+    if _dtype_code(q) != ATTN_E4M3:
+        raise TypeError("attn_fwd_fp8 takes e4m3 codes (uint8 or float8_e4m3fn)")
+    o, lse = _outputs(q, o, lse, B, H, N, d, ATTN_E4M3)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    lib = load_library()
+    _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                            scale, float(q_descale), float(k_descale), float(v_descale), int(bool(causal)),
+                            _stream_handle(stream, q.device)))
+    return o, lse
+
+
+def attn_fwd_host(h_q, h_k, h_v, h_o, h_lse, d_q, d_k, d_v, d_o, d_lse, scale=None, causal=False,
+                  descales=(1.0, 1.0, 1.0), stream=None):
+    """End-to-end forward from (page-locked) host tensors through caller-owned
+    device staging tensors: H2D copies, forward, D2H copies, all enqueued on
+    `stream`.  The caller synchronises before reading h_o / h_lse."""
+    B, H, N, d = (int(x) for x in h_q.shape)
+    code = _dtype_code(h_q)
+    for t in (d_q, d_k, d_v, d_o, d_lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("device staging tensors must be contiguous CUDA tensors")
+    for t in (h_q, h_k, h_v, h_o, h_lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    lib = load_library()
+    _check(lib.attn_fwd_host(h_q.data_ptr(), h_k.data_ptr(), h_v.data_ptr(), h_o.data_ptr(), h_lse.data_ptr(),
+                             d_q.data_ptr(), d_k.data_ptr(), d_v.data_ptr(), d_o.data_ptr(), d_lse.data_ptr(),
+                             B, H, N, d, scale, float(descales[0]), float(descales[1]), float(descales[2]),
+                             int(bool(causal)), code, _stream_handle(stream, d_q.device)))
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise and return the device status (0 = ok, 5 = a wait timed out)."""
+    lib = load_library()
+    return int(lib.attn_get_device_status(_stream_handle(stream, None)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(load_library().attn_set_wait_limit_ns(int(ns)))
+
+
+def forward(q, k, v, causal=False, scale=None, descales=None):
+    """Convenience: dispatch on dtype (e4m3 needs `descales`)."""
+    if _dtype_code(q) == ATTN_E4M3 and descales is not None:
+        return attn_fwd_fp8(q, k, v, *descales, scale=scale, causal=causal)
+    return attn_fwd(q, k, v, scale=scale, causal=causal)

@@ -1,0 +1,262 @@
+// C-ABI layer of libattn_fa2.so: argument validation, TMA descriptor encoding,
+// kernel selection and launch, device status word.  The entry points are
+// declared (with their contracts) in include/attn_fa2.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "attn_fa2.h"
+#include "attn_kernels.h"
+
+namespace {
+
+// Device status word: a kernel that gives up on a wait writes ATTN_ERR_TIMEOUT here.
+__device__ int g_attn_status = 0;
+
+thread_local char g_last_error[256] = "";
+uint64_t g_wait_limit_ns = 2000000000ull;
+
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Address of the status word on the current device (looked up once per device).
+int status_ptr(int** out) {
+  constexpr int kMaxDev = 64;
+  static int* cache[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDev) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    cache[dev] = static_cast<int*>(p);
+  }
+  *out = cache[dev];
+  return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH, N, d] tensor: dims (d, N, BH), 128-row boxes of one
+// 128-byte column block, 128-byte swizzle, zero fill outside [0, N).
+int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                                 static_cast<cuuint64_t>(N) * d * elem_bytes};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+                 int N, int d, float scale, int causal) {
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+  if (B < 1 || H < 1 || N < 1 || d < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d H=%d N=%d d=%d)", B, H, N, d);
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return fail(ATTN_ERR_INVALID_ARG, "B*H overflows int");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", double(scale));
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(ATTN_ERR_MISALIGNED, "q, k, v and o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(ATTN_ERR_MISALIGNED, "lse must be 4-byte aligned");
+  return ATTN_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, float qds, float kds, float vds, int causal, bool fp8, cudaStream_t stream) {
+  if (fp8 ? (d != 128) : (d != 64 && d != 128))
+    return fail(ATTN_ERR_UNSUPPORTED, "%s tensor-core path supports d in %s (got %d)", fp8 ? "e4m3" : "bf16",
+                fp8 ? "{128}" : "{64, 128}", d);
+  const int BH = B * H;
+  const long long n_pairs = (static_cast<long long>(N) + 255) / 256;
+  if (n_pairs * BH > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "grid too large (B*H*ceil(N/256))");
+  attn::TcParams p;
+  std::memset(&p, 0, sizeof(p));
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int eb = fp8 ? 1 : 2;
+  int st;
+  if ((st = make_map(&p.tm_q, q, dt, eb, BH, N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_k, k, dt, eb, BH, N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, dt, eb, BH, N, d)) != ATTN_OK) return st;
+  if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
+  p.o = o;
+  p.lse = lse;
+  p.BH = BH;
+  p.N = N;
+  p.n_pairs = static_cast<int>(n_pairs);
+  p.scale_log2 = scale * kLog2e * qds * kds;
+  p.o_scale = vds;
+  p.timeout_ns = g_wait_limit_ns;
+  cudaError_t e = fp8 ? attn::launch_tc_e4m3(p, d, causal != 0, stream) : attn::launch_tc_bf16(p, d, causal != 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ATTN_OK;
+}
+
+int run_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal, cudaStream_t stream) {
+  if (d != 16 && d != 32 && d != 64 && d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "fp32 path supports d in {16, 32, 64, 128} (got %d)", d);
+  attn::SimtParams p;
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<float*>(o);
+  p.lse = lse;
+  p.BH = B * H;
+  p.N = N;
+  p.scale_log2 = scale * kLog2e;
+  cudaError_t e = attn::launch_simt_f32(p, d, causal != 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ATTN_OK;
+}
+
+int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, float qds, float kds, float vds, int causal, int dtype, cudaStream_t stream) {
+  int st = check_common(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  switch (dtype) {
+    case ATTN_F32: return run_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+    case ATTN_BF16: return run_tc(q, k, v, o, lse, B, H, N, d, scale, 1.f, 1.f, 1.f, causal, false, stream);
+    case ATTN_E4M3: return run_tc(q, k, v, o, lse, B, H, N, d, scale, qds, kds, vds, causal, true, stream);
+    default: return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  }
+}
+
+bool good_descale(float x) { return x > 0.f && std::isfinite(x); }
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, int causal, int dtype, void* stream) {
+  g_last_error[0] = '\0';
+  return dispatch(q, k, v, o, lse, B, H, N, d, scale, 1.f, 1.f, 1.f, causal, dtype,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, float q_descale, float k_descale, float v_descale, int causal, void* stream) {
+  g_last_error[0] = '\0';
+  if (!good_descale(q_descale) || !good_descale(k_descale) || !good_descale(v_descale))
+    return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
+  return dispatch(q, k, v, o, lse, B, H, N, d, scale, q_descale, k_descale, v_descale, causal, ATTN_E4M3,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_host(const void* h_q, const void* h_k, const void* h_v, void* h_o, float* h_lse, void* d_q,
+                  void* d_k, void* d_v, void* d_o, float* d_lse, int B, int H, int N, int d, float scale,
+                  float q_descale, float k_descale, float v_descale, int causal, int dtype, void* stream) {
+  g_last_error[0] = '\0';
+  if (!h_q || !h_k || !h_v || !h_o || !h_lse) return fail(ATTN_ERR_INVALID_ARG, "null host pointer");
+  int st = check_common(d_q, d_k, d_v, d_o, d_lse, B, H, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_E4M3)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (dtype == ATTN_E4M3 && (!good_descale(q_descale) || !good_descale(k_descale) || !good_descale(v_descale)))
+    return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
+  const size_t in_elem = dtype == ATTN_F32 ? 4 : (dtype == ATTN_BF16 ? 2 : 1);
+  const size_t out_elem = dtype == ATTN_F32 ? 4 : 2;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t in_bytes = rows * d * in_elem;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(d_q, h_q, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy q");
+  if ((e = cudaMemcpyAsync(d_k, h_k, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy k");
+  if ((e = cudaMemcpyAsync(d_v, h_v, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess) return cuda_fail(e, "copy v");
+  const bool fp8 = dtype == ATTN_E4M3;
+  st = dispatch(d_q, d_k, d_v, d_o, d_lse, B, H, N, d, scale, fp8 ? q_descale : 1.f, fp8 ? k_descale : 1.f,
+                fp8 ? v_descale : 1.f, causal, dtype, s);
+  if (st != ATTN_OK) return st;
+  if ((e = cudaMemcpyAsync(h_o, d_o, rows * d * out_elem, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy o");
+  if ((e = cudaMemcpyAsync(h_lse, d_lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy lse");
+  return ATTN_OK;
+}
+
+int attn_get_device_status(void* stream) {
+  g_last_error[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int* dptr = nullptr;
+  int st = status_ptr(&dptr);
+  if (st != ATTN_OK) return st;
+  int h = 0;
+  if ((e = cudaMemcpy(&h, dptr, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status");
+  if (h != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpy(dptr, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear status");
+    return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a device-side wait");
+  }
+  return ATTN_OK;
+}
+
+uint64_t attn_set_wait_limit_ns(uint64_t ns) {
+  const uint64_t old = g_wait_limit_ns;
+  g_wait_limit_ns = ns < 1000000ull ? 1000000ull : ns;
+  return old;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* attn_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal interface between the C-ABI layer (attn_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Arguments of the tensor-core forward kernels (bf16 and e4m3 inputs).
+// Q, K, V are [B, H, N, d] row-major and reached only through the TMA
+// descriptors; O ([B, H, N, d] bf16) and L ([B, H, N] fp32) are written with
+// plain stores.
+struct TcParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;              // bf16 [BH, N, d]
+  float* lse;           // fp32 [BH, N], natural log
+  int* status;          // device status word (timeouts)
+  int BH;               // B * H
+  int N;                // sequence length (queries = keys)
+  int n_pairs;          // ceil(N / 256): CTAs per head (two 128-row query tiles each)
+  float scale_log2;     // softmax scale * log2(e) * q_descale * k_descale
+  float o_scale;        // v_descale / P multiplier (1 for bf16, v_descale/256 for e4m3)
+  unsigned long long timeout_ns;
+};
+
+// Arguments of the SIMT fp32 forward kernel.
+struct SimtParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;
+  float* lse;
+  int BH;
+  int N;
+  float scale_log2;     // softmax scale * log2(e)
+};
+
+// Launchers (defined next to their kernels).  Return the launch error.
+cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, cudaStream_t stream);
+cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, cudaStream_t stream);
+cudaError_t launch_simt_f32(const SimtParams& p, int d, bool causal, cudaStream_t stream);
+
+}  // namespace attn

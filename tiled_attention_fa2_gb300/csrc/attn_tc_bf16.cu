@@ -1,0 +1,12 @@
+// bf16 instances of the tcgen05 forward kernel (d = 64, 128; causal or not).
+#include "attn_tc_sm103.cuh"
+
+namespace attn {
+
+cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, cudaStream_t stream) {
+  if (d == 128) return causal ? launch_tc<TcCfg<false, 128, true>>(p, stream) : launch_tc<TcCfg<false, 128, false>>(p, stream);
+  if (d == 64) return causal ? launch_tc<TcCfg<false, 64, true>>(p, stream) : launch_tc<TcCfg<false, 64, false>>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

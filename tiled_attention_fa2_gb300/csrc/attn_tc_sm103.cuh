@@ -1,0 +1,383 @@
+// FlashAttention-2-style fused attention forward for sm_103a on the fifth-
+// generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// What it computes follows "FlashAttention-2 from PyTorch to Triton" (the FA2
+// forward pass: per query tile, stream key/value tiles, keep running m, l and
+// an unnormalised O rescaled by exp(m_old - m_new), divide by l once at the
+// end and write L = m + log l) and "1.8x Faster Attention on an RTX 5080: an
+// FP8 Flash Attention Kernel in CuTe-DSL" (FP8 descales folded into the score
+// scale, P scaled by 256 before the FP8 cast).  How it runs is GB300-first:
+//
+//   * one CTA = two 128-row query tiles of one (batch, head); the two tiles
+//     ping-pong so the tensor core runs one tile's GEMM while the other tile's
+//     softmax runs on the CUDA cores ("Kernels and Memory in LLM Inference",
+//     FlashAttention-3/-4 sections: overlap the two jobs);
+//   * warp specialisation: warps 0-3 and 4-7 are the softmax warpgroups of
+//     tile 0 and tile 1 (thread r owns query row r: TMEM lane r), warp 8 is the
+//     TMA producer, warp 9 allocates TMEM and issues every tcgen05.mma;
+//   * S = Q K^T accumulates in TMEM (128 fp32 columns per tile); P (bf16 or
+//     e4m3) is written back over the same columns and used as the A operand of
+//     O += P V straight from TMEM; O (d fp32 columns per tile) stays in TMEM
+//     for the whole key loop.  512 columns: S0 | S1 | O0 | O1;
+//   * K and V stream through one ring of 128-key shared-memory slots
+//     (K0, V0, K1, V1, ...) with full/empty mbarriers;
+//   * exp2 with scale*log2(e) folded into one FFMA per score; the O rescale is
+//     skipped for a warp whose 32 rows all kept their max;
+//   * causal: only key tiles up to the diagonal are visited, the mask is
+//     applied on the diagonal tile only, and heavy query tiles launch first;
+//     a ragged last key tile is masked (keys >= N are not phantom zeros).
+#pragma once
+
+#include "attn_kernels.h"
+#include "ptx_sm103.cuh"
+
+namespace attn {
+
+template <bool kFp8, int kD, bool kCausal>
+struct TcCfg {
+  static constexpr bool kIsFp8 = kFp8;
+  static constexpr int D = kD;
+  static constexpr bool kCaus = kCausal;
+  static constexpr int kElem = kFp8 ? 1 : 2;                 // bytes per element
+  static constexpr int kRowBytes = kD * kElem;               // bytes per tile row
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
+  static constexpr int kBlocks = kRowBytes / 128;            // 128-byte column blocks per row
+  static constexpr int kBoxCols = 128 / kElem;               // elements per 128-byte block
+  static constexpr int kBlockBytes = 128 * 128;              // one column block of a 128-row tile
+  static constexpr int kTileBytes = 128 * kRowBytes;         // one 128-row tile
+  static constexpr int kMmaK = kFp8 ? 32 : 16;               // K of one tcgen05.mma
+  static constexpr int kQkSteps = kD / kMmaK;
+  static constexpr int kPvSteps = 128 / kMmaK;
+  static constexpr int kStages = (kTileBytes == 32768) ? 5 : 8;
+  static constexpr int kPCols = kFp8 ? 32 : 64;              // TMEM columns of one P tile
+  static constexpr float kPExp = kFp8 ? 8.f : 0.f;           // P is stored as p * 2^kPExp
+  static constexpr uint32_t kFmt = kFp8 ? 0u : 1u;
+  static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
+  static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, kD, 0, 1);
+  static constexpr int kQBytes = 2 * kTileBytes;
+  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol0 = 256;
+};
+
+
+template <int kCols>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kCols]) {
+  if constexpr (kCols == 128) tmem_ld128_sync(taddr, r);
+  else if constexpr (kCols == 64) tmem_ld64_sync(taddr, r);
+  else tmem_ld32_sync(taddr, r);
+}
+template <int kCols>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[kCols]) {
+  if constexpr (kCols == 128) tmem_st128_sync(taddr, r);
+  else if constexpr (kCols == 64) tmem_st64_sync(taddr, r);
+  else tmem_st32_sync(taddr, r);
+}
+
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_base, uint32_t k_base) {
+#pragma unroll
+  for (int kk = 0; kk < C::kQkSteps; ++kk) {
+    const uint32_t byte = kk * C::kMmaK * C::kElem;                 // offset inside a row
+    const uint32_t off = (byte / 128) * C::kBlockBytes + (byte % 128);
+    const uint64_t a = sdesc_sw128(q_base + off, 16, 1024);
+    const uint64_t b = sdesc_sw128(k_base + off, 16, 1024);
+    if constexpr (C::kIsFp8) mma_f8_ss(tmem_s, a, b, C::kIdescQK, kk > 0);
+    else mma_f16_ss(tmem_s, a, b, C::kIdescQK, kk > 0);
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < C::kPvSteps; ++kk) {
+    // V slot: key rows of 128 bytes per column block; the B operand is MN-major
+    // (d contiguous): SBO = 8 key rows, LBO = next 128-byte column block.
+    const uint64_t b = sdesc_sw128(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 1024);
+    const uint32_t a = tmem_p + kk * 8;  // kMmaK elements of P = 8 TMEM columns
+    if constexpr (C::kIsFp8) mma_f8_ts(tmem_o, a, b, C::kIdescPV, accumulate || kk > 0);
+    else mma_f16_ts(tmem_o, a, b, C::kIdescPV, accumulate || kk > 0);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+
+  const uint32_t q_base = base;
+  const uint32_t slot_base = base + C::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBarOff);
+  // barrier layout: [0] q_full, [1..S] slot_full, [S+1..2S] slot_empty,
+  // then s_full[2], p_full[2], o_full[2], mma_done
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
+  const int kS = C::kStages;
+  const uint32_t q_full = bar(0);
+  auto slot_full = [&](int s) { return bar(1 + s); };
+  auto slot_empty = [&](int s) { return bar(1 + kS + s); };
+  auto s_full = [&](int t) { return bar(1 + 2 * kS + t); };
+  auto p_full = [&](int t) { return bar(3 + 2 * kS + t); };
+  auto o_full = [&](int t) { return bar(5 + 2 * kS + t); };
+  const uint32_t mma_done = bar(7 + 2 * kS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8 + 2 * kS);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- tile coordinates
+  int bh, pair;
+  if constexpr (C::kCaus) {
+    pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH;  // heaviest query tiles first
+    bh = static_cast<int>(blockIdx.x) % p.BH;
+  } else {
+    bh = static_cast<int>(blockIdx.x) / p.n_pairs;
+    pair = static_cast<int>(blockIdx.x) % p.n_pairs;
+  }
+  const int N = p.N;
+  const int n_kt = (N + 127) >> 7;
+  int kv_end0 = n_kt, kv_end1 = n_kt;
+  if constexpr (C::kCaus) {
+    kv_end0 = min(2 * pair + 1, n_kt);
+    kv_end1 = min(2 * pair + 2, n_kt);
+  }
+  const int n_kv = kv_end1;  // key tiles visited by the CTA (tile 1 needs >= tile 0)
+
+  // ---- setup: barriers, TMEM
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(slot_full(s), 1);
+      mbar_init(slot_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), 128);
+      mbar_init(o_full(t), 1);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+  const uint64_t lim = p.timeout_ns;
+
+  if (warp == 8) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      for (int t = 0; t < 2; ++t) {
+        // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
+        // its results are never stored.
+        const int y = (2 * pair + t) * 128 < N ? (2 * pair + t) * 128 : 0;
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int j = it >> 1;
+        const int s = it % kS;
+        const uint32_t ph = (it / kS) & 1;
+        if (!mbar_wait(slot_empty(s), ph ^ 1u, p.status, lim)) break;
+        mbar_arrive_expect_tx(slot_full(s), C::kTileBytes);
+        const CUtensorMap* map = (it & 1) ? &p.tm_v : &p.tm_k;
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
+                      j * 128, bh);
+        ++issued;
+      }
+      // Drain: every copy this thread issued has landed before the CTA may exit.
+      mbar_wait(q_full, 0, p.status, lim);
+      for (int it = max(0, issued - kS); it < issued; ++it)
+        mbar_wait(slot_full(it % kS), (it / kS) & 1, p.status, lim);
+    }
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, p.status, lim);
+      int it = 0;  // ring position of the next K/V tile
+      // S_t = Q_t K_0^T for both tiles
+      if (ok) ok = mbar_wait(slot_full(0), 0, p.status, lim);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t kb = slot_base;
+        issue_qk<C>(tmem + 0, q_base, kb);
+        mma_commit(s_full(0));
+        issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
+        mma_commit(s_full(1));
+        mma_commit(slot_empty(0));
+        it = 1;
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int sv = it % kS;
+        ok = mbar_wait(slot_full(sv), (it / kS) & 1, p.status, lim);
+        if (!ok) break;
+        const int itk = it + 1;
+        const int sk = itk % kS;
+        const bool next = (j + 1 < n_kv);
+        bool k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int kv_end = t ? kv_end1 : kv_end0;
+          if (j < kv_end) {
+            ok = mbar_wait(p_full(t), j & 1, p.status, lim);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<C>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, slot_base + sv * C::kTileBytes, j > 0);
+            mma_commit(o_full(t));
+          }
+          if (t == 1) mma_commit(slot_empty(sv));
+          if (j + 1 < kv_end) {
+            if (!k_ready) {
+              ok = mbar_wait(slot_full(sk), (itk / kS) & 1, p.status, lim);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
+            mma_commit(s_full(t));
+          }
+        }
+        if (!ok) break;
+        if (next) mma_commit(slot_empty(sk));
+        it += 2;
+      }
+      // Every MMA issued by this thread has completed before TMEM is freed.
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, p.status, lim);
+    }
+  } else {
+    // ================================================================ softmax warpgroups
+    const int t = tid >> 7;                      // query tile of this warpgroup
+    const int r = tid & 127;                     // row inside the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + t * 128;
+    const uint32_t t_o = tmem + lane_base + C::kOCol0 + t * C::D;
+    const int qt = 2 * pair + t;
+    const int row = qt * 128 + r;
+    const int kv_end = t ? kv_end1 : kv_end0;
+    const float sl2 = p.scale_log2;
+    float m2 = -INFINITY;  // running max of s * sl2 (log2 domain)
+    float l = 0.f;         // running sum of p * 2^kPExp
+    bool ok = true;
+
+    for (int j = 0; j < kv_end; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, p.status, lim));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t u[128];
+      tmem_ld128_sync(t_s, u);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+      const bool diag = C::kCaus && (j == qt);
+      const bool ragged = (j == n_kt - 1) && ((N & 127) != 0);
+      if (diag || ragged) {
+        const int key0 = j * 128;
+        const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (key0 + c > lim_key) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m2, mx * sl2);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m2 - m_use);
+      const float neg = C::kPExp - m_use;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        s[c] = ex2_approx(fmaf(s[c], sl2, neg));
+        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, neg));
+        rs0 += s[c];
+        rs1 += s[c + 1];
+      }
+      l = fmaf(l, alpha, rs0 + rs1);
+      // P goes over the S columns this thread has already consumed.
+      if constexpr (C::kIsFp8) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+        tmem_st32_sync(t_s, pk);
+      } else {
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+        tmem_st64_sync(t_s, pk);
+      }
+      if (j > 0) {
+        // O still holds the sum up to key tile j-1 at the old max: rescale by alpha.
+        ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), (j - 1) & 1, p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t o[C::D];
+          tmem_ld_cols<C::D>(t_o, o);
+#pragma unroll
+          for (int i = 0; i < C::D; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_cols<C::D>(t_o, o);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(p_full(t));
+      m2 = m_new;
+    }
+
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), (kv_end - 1) & 1, p.status, lim));
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = p.o_scale / l;
+      const bool live = row < N;
+      uint32_t o[C::D];
+      tmem_ld_cols<C::D>(t_o, o);
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                              (static_cast<size_t>(bh) * N + row) * C::D);
+#pragma unroll
+        for (int i = 0; i < C::D / 8; ++i) {
+          const float* f = reinterpret_cast<const float*>(o) + 8 * i;
+          dst[i] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                              pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+        }
+        p.lse[static_cast<size_t>(bh) * N + row] = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <class C>
+cudaError_t launch_tc(const TcParams& p, cudaStream_t stream) {
+  auto kern = attn_fwd_tc_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.BH) * p.n_pairs;
+  kern<<<dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
