@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Throughput of the attention forward on GB300: one JSON line.
+
+A step is one attention forward (every step of the fused path, in one kernel)
+over one batch of the workload.  Default workload: bf16 causal LM prefill,
+B=4, H=16, N=2048, d=128.  Inputs are resident in HBM before timing; L2 is
+flushed (a 512 MiB device write) before every timed step, outside the timed
+interval; each step is timed with CUDA events on the stream the kernel runs
+on, and the sum over the K steps gives the throughput.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 oracle on the host cores
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica of
+the workload (attention heads are independent, no data-path collective), the
+slowest rank's time is used, and `value` counts the work of all ranks (weak
+scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from tiled_attention_fa2_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS & % of GB300 dense bf16/fp8 tensor peak; ms per call"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "prefill_causal_bf16"
+FLUSH_BYTES = 512 << 20
+# Published figures for an exact workload (other hardware: context only).
+PUBLISHED_TFLOPS = {"dit_e4m3": 26.27e12 / 123.6e-3 / 1e12}  # RTX 5080, final FP8 CuTe-DSL kernel
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "tiled_attention_fa2_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def dtype_peak(dtype: str, peaks: dict):
+    """Dense tensor peak for the contraction dtype: bf16 measured (cuBLAS burst);
+    e4m3 = bf16 x 2 (nominal fp8:bf16 ratio); f32 runs on the CUDA cores."""
+    if dtype == "e4m3":
+        return 2.0 * peaks["bf16_tflops"], "bf16 burst x 2 (nominal fp8/bf16 ratio)"
+    return peaks["bf16_tflops"], "bf16 burst"
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch from an ncu capture of the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    e = t.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_device_inputs(w: dict, device, seed: int):
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=w["q_mult"])
+    descales = (1.0, 1.0, 1.0)
+    if w["dtype"] == "bf16":
+        host = tuple(inputs.to_bf16(t) for t in (q, k, v))
+    elif w["dtype"] == "e4m3":
+        qs, ks, vs = (inputs.quantize_e4m3(t) for t in (q, k, v))
+        host = (qs[0], ks[0], vs[0])
+        descales = (qs[1], ks[1], vs[1])
+    else:
+        host = (q, k, v)
+    return host, tuple(t.to(device) for t in host), descales
+
+
+def run_gpu_arm(args, w):
+    from tiled_attention_fa2_gb300 import binding
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    lib = binding.load_library()
+
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    host, (q, k, v), descales = make_device_inputs(w, device, seed=rank)
+    code = {"f32": 0, "bf16": 1, "e4m3": 2}[w["dtype"]]
+    odt = torch.float32 if code == 0 else torch.bfloat16
+    o = torch.empty((B, H, N, d), dtype=odt, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def launch():
+        if code == 2:
+            st = lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                  scale, *descales, int(causal), sh)
+        else:
+            st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              scale, int(causal), code, sh)
+        if st != 0:
+            raise RuntimeError(lib.attn_last_error().decode())
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        launch()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    time.sleep(0.2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        launch()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    st = binding.get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(times_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = inputs.attention_flops(B, H, N, d, causal)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    mean_ms = total_ms / args.steps
+
+    # ---- end to end: pinned host buffers through the C ABI (copies inside the timed region)
+    e2e_steps = max(1, min(args.steps, 20))
+    h_in = [t.pin_memory() for t in host]
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_l = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    d_in = [torch.empty_like(t) for t in (q, k, v)]
+
+    def e2e_call():
+        st = lib.attn_fwd_host(h_in[0].data_ptr(), h_in[1].data_ptr(), h_in[2].data_ptr(), h_o.data_ptr(),
+                               h_l.data_ptr(), d_in[0].data_ptr(), d_in[1].data_ptr(), d_in[2].data_ptr(),
+                               o.data_ptr(), lse.data_ptr(), B, H, N, d, scale, *descales, int(causal), code, sh)
+        if st != 0:
+            raise RuntimeError(lib.attn_last_error().decode())
+
+    e2e_call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    in_bytes = sum(t.numel() * t.element_size() for t in host)
+    out_bytes = o.numel() * o.element_size() + lse.numel() * 4
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks, peaks_src = load_peaks()
+    peak, peak_note = dtype_peak(w["dtype"], peaks)
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 5),
+        "ms_per_step_median": round(statistics.median(times_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / PUBLISHED_TFLOPS[args.workload], 3) if args.workload in PUBLISHED_TFLOPS else None,
+        "dtype": w["dtype"],
+        "data": "synthetic: i.i.d. N(0,1) Q/K/V from a seeded CPU generator (seed = rank)",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": bool(causal),
+                   "flops_per_step": flops, "l2": "flushed before every timed step (512 MiB device write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peaks_src}: {peak_note}",
+                     "traffic": profile_traffic(args.workload)},
+        "clocks": clocks,
+        "e2e": {"value": round(flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes},
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, host, descales, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _oracle_head_inputs(w, host, descales, h):
+    import oracle
+
+    fmt = w["dtype"]
+    BHN = (w["B"] * w["H"], w["N"], w["d"])
+    out = []
+    for t, ds in zip(host, descales):
+        if fmt == "bf16":
+            c = inputs.bits_u16(t).reshape(BHN)[h]
+        elif fmt == "e4m3":
+            c = inputs.bits_u8(t).reshape(BHN)[h]
+        else:
+            c = t.reshape(BHN)[h].numpy()
+        out.append(oracle.dequantize(c, fmt, ds))
+    return out
+
+
+def oracle_sample(w, host, descales, heads, rows_per_head):
+    """Oracle on a sample: the first `rows_per_head` query rows (in seeded
+    sample order) of the given heads.  Returns (seconds, flops of the sample)."""
+    import oracle
+
+    N, d, causal = w["N"], w["d"], w["causal"]
+    rows = inputs.sample_rows(N, w["B"], w["H"], count=min(N, max(rows_per_head, 2)))
+    flops = 0.0
+    t0 = time.perf_counter()
+    for h in heads:
+        q, k, v = _oracle_head_inputs(w, host, descales, h)
+        r = rows[h][None]
+        oracle.attention_rows(q[None], k[None], v[None], r, 1 / math.sqrt(d), causal)
+        keys = (r[0] + 1) if causal else np.full(r.shape[1], N)
+        flops += float(4.0 * d * keys.sum())
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(w, host, descales, budget_s=15.0):
+    """Time the oracle as it stands on this host's cores, on a bounded sample."""
+    BH = w["B"] * w["H"]
+    rows = min(w["N"], 512)
+    secs, flops = oracle_sample(w, host, descales, [0], rows)
+    heads = [0]
+    if secs < budget_s:
+        n = max(1, min(BH, int(budget_s / max(secs, 1e-3))))
+        heads = list(range(n))
+        secs, flops = oracle_sample(w, host, descales, heads, rows)
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(heads)} of {BH} heads x {rows} sampled query rows (causal rows see keys <= row); "
+                      f"{secs:.1f} s; numpy float64, BLAS threads = all cores",
+            "seconds": round(secs, 2)}
+
+
+def run_reference_arm(args, w):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload (one head x 512 sampled rows) timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    host, descales = make_host_inputs(w)
+    BH = w["B"] * w["H"]
+    rows = min(w["N"], 512)
+    for i in range(args.warmup):
+        oracle_sample(w, host, descales, [i % BH], rows)
+    tot_s, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        s, f = oracle_sample(w, host, descales, [i % BH], rows)
+        tot_s += s
+        tot_f += f
+    value = tot_f / tot_s / 1e12
+    sample = f"each step: 1 head x {rows} sampled query rows of the workload; numpy float64, BLAS threads = all cores"
+    line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same recipe as the GPU arm)",
+            "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
+                       "causal": bool(w["causal"])},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def make_host_inputs(w):
+    q, k, v = inputs.make_qkv_f32(w["B"], w["H"], w["N"], w["d"], seed=0, q_mult=w["q_mult"])
+    if w["dtype"] == "bf16":
+        return tuple(inputs.to_bf16(t) for t in (q, k, v)), (1.0, 1.0, 1.0)
+    if w["dtype"] == "e4m3":
+        qs, ks, vs = (inputs.quantize_e4m3(t) for t in (q, k, v))
+        return (qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])
+    return (q, k, v), (1.0, 1.0, 1.0)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference_arm(args, w)
+    else:
+        run_gpu_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()
