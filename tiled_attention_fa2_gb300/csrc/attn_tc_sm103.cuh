@@ -50,7 +50,11 @@ struct TcCfg {
   static constexpr int kPvSteps = 128 / kMmaK;
   static constexpr int kStages = (kTileBytes == 32768) ? 5 : 8;
   static constexpr int kPCols = kFp8 ? 32 : 64;              // TMEM columns of one P tile
-  static constexpr float kPExp = kFp8 ? 8.f : 0.f;           // P is stored as p * 2^kPExp
+  // Conditional rescale: the reference max used in the exponentials moves only
+  // when the row max grows by more than kTau (log2 units), so p <= 2^kTau.
+  // P is stored as p * 2^kPExp; for e4m3 2^(kTau + kPExp) = 256 <= 448 (max finite).
+  static constexpr float kTau = kFp8 ? 4.f : 8.f;
+  static constexpr float kPExp = kFp8 ? 4.f : 0.f;
   static constexpr uint32_t kFmt = kFp8 ? 0u : 1u;
   static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, kD, 0, 1);
@@ -292,22 +296,41 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         for (int c = 0; c < 128; ++c)
           if (key0 + c > lim_key) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row max: eight independent three-input max chains, then a short tree.
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m2, mx * sl2);
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+      for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          mx8[i] = fmax3(mx8[i], s[c + i], s[c + i + 1]);
+          mx8[i + 1] = fmax3(mx8[i + 1], s[c + i + 8], s[c + i + 9]);
+        }
+      }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      // Reference max: moves only when the row max grew by more than kTau (then
+      // O and l are rescaled); otherwise p may exceed 1 by at most 2^kTau.
+      const float m_cand = fmaxf(m2, mx * sl2);
+      const float m_new = (m_cand > m2 + C::kTau) ? m_cand : m2;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m2 - m_use);
-      const float neg = C::kPExp - m_use;
-      float rs0 = 0.f, rs1 = 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
+      uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, neg));
-        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, neg));
-        rs0 += s[c];
-        rs1 += s[c + 1];
+      for (int c = 0; c < 128; c += 4) {
+        const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2);
+        const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negx2);
+        s[c] = ex2_approx(f2_lo(a));
+        s[c + 1] = ex2_approx(f2_hi(a));
+        s[c + 2] = ex2_approx(f2_lo(b));
+        s[c + 3] = ex2_approx(f2_hi(b));
+        rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
+        rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
       }
-      l = fmaf(l, alpha, rs0 + rs1);
+      const uint64_t rs = f2_add(rs0, rs1);
+      l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
       // P goes over the S columns this thread has already consumed.
       if constexpr (C::kIsFp8) {
         uint32_t pk[32];
@@ -328,8 +351,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t o[C::D];
           tmem_ld_cols<C::D>(t_o, o);
+          const uint64_t ax2 = f2_pack(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < C::D; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < C::D; i += 2) {
+            const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2);
+            o[i] = static_cast<uint32_t>(v);
+            o[i + 1] = static_cast<uint32_t>(v >> 32);
+          }
           tmem_st_cols<C::D>(t_o, o);
         }
       }
