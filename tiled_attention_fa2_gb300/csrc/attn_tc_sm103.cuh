@@ -59,7 +59,7 @@ struct TcCfg {
   static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, kD, 0, 1);
   static constexpr int kQBytes = 2 * kTileBytes;
-  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;
+  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 10 barriers + TMEM holder
   static constexpr int kSmemBytes = kBarOff + 1024 /*barriers*/ + 1024 /*alignment slack*/;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -88,23 +88,74 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_base, uint3
     const uint32_t off = (byte / 128) * C::kBlockBytes + (byte % 128);
     const uint64_t a = sdesc_sw128(q_base + off, 16, 1024);
     const uint64_t b = sdesc_sw128(k_base + off, 16, 1024);
-    if constexpr (C::kIsFp8) mma_f8_ss(tmem_s, a, b, C::kIdescQK, kk > 0);
-    else mma_f16_ss(tmem_s, a, b, C::kIdescQK, kk > 0);
+    if constexpr (C::kIsFp8) mma_f8_ss_elect(tmem_s, a, b, C::kIdescQK, kk > 0);
+    else mma_f16_ss_elect(tmem_s, a, b, C::kIdescQK, kk > 0);
   }
 }
 
-template <class C>
+// One half (keys [64h, 64h + 64)) of O += P V.
+template <class C, int kHalf>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base, bool accumulate) {
+  constexpr int kSteps = C::kPvSteps / 2;
 #pragma unroll
-  for (int kk = 0; kk < C::kPvSteps; ++kk) {
+  for (int i = 0; i < kSteps; ++i) {
+    const int kk = kHalf * kSteps + i;
     // V slot: key rows of 128 bytes per column block; the B operand is MN-major
     // (d contiguous): SBO = 8 key rows, LBO = next 128-byte column block.
     const uint64_t b = sdesc_sw128(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 1024);
     const uint32_t a = tmem_p + kk * 8;  // kMmaK elements of P = 8 TMEM columns
-    if constexpr (C::kIsFp8) mma_f8_ts(tmem_o, a, b, C::kIdescPV, accumulate || kk > 0);
-    else mma_f16_ts(tmem_o, a, b, C::kIdescPV, accumulate || kk > 0);
+    if constexpr (C::kIsFp8) mma_f8_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
+    else mma_f16_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
   }
 }
+
+// Exponentials of keys [64h, 64h + 64) of this thread's score row, their
+// packed row sums, and P for those keys written to TMEM over the S columns
+// already consumed (bf16: 32 columns at 32h; e4m3: 16 columns at 16h).
+template <class C, int kHalf>
+__device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, uint64_t negx2, uint64_t& rs0,
+                                             uint64_t& rs1, uint32_t t_s) {
+#pragma unroll
+  for (int c = 64 * kHalf; c < 64 * kHalf + 64; c += 4) {
+    const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2);
+    const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negx2);
+    s[c] = ex2_approx(f2_lo(a));
+    s[c + 1] = ex2_approx(f2_hi(a));
+    s[c + 2] = ex2_approx(f2_lo(b));
+    s[c + 3] = ex2_approx(f2_hi(b));
+    rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
+    rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
+  }
+  if constexpr (C::kIsFp8) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = 64 * kHalf + 4 * i;
+      pk[i] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+    }
+    tmem_st16_sync(t_s + 16 * kHalf, pk);
+  } else {
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 * kHalf + 2 * i], s[64 * kHalf + 2 * i + 1]);
+    tmem_st32_sync(t_s + 32 * kHalf, pk);
+  }
+}
+
+// Optional event trace (compile with -DATTN_TRACE): per-CTA cycle stamps of
+// the pipeline hand-offs of one chosen CTA, for timeline analysis.
+#ifdef ATTN_TRACE
+static __device__ unsigned long long g_attn_trace[8 * 64 * 8];
+static __device__ int g_attn_trace_cta = 0;
+#define ATTN_TRACE_EV(on, role, j, ev)                                                      \
+  do {                                                                                      \
+    if ((on) && (j) < 64) g_attn_trace[((role) * 64 + (j)) * 8 + (ev)] = clock64();        \
+  } while (0)
+#else
+#define ATTN_TRACE_EV(on, role, j, ev) \
+  do {                                 \
+  } while (0)
+#endif
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
@@ -116,23 +167,29 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
   const uint32_t q_base = base;
   const uint32_t slot_base = base + C::kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBarOff);
-  // barrier layout: [0] q_full, [1..S] slot_full, [S+1..2S] slot_empty,
-  // then s_full[2], p_full[2], o_full[2], mma_done
+  // barrier layout: q_full | slot_full[S] | slot_empty[S] | s_full[2] | p_lo[2] | p_hi[2] | o_full[2] | mma_done
   const uint32_t bar0 = smem_u32(bars);
-  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   const int kS = C::kStages;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   const uint32_t q_full = bar(0);
   auto slot_full = [&](int s) { return bar(1 + s); };
   auto slot_empty = [&](int s) { return bar(1 + kS + s); };
   auto s_full = [&](int t) { return bar(1 + 2 * kS + t); };
-  auto p_full = [&](int t) { return bar(3 + 2 * kS + t); };
-  auto o_full = [&](int t) { return bar(5 + 2 * kS + t); };
-  const uint32_t mma_done = bar(7 + 2 * kS);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8 + 2 * kS);
+  auto p_lo = [&](int t) { return bar(3 + 2 * kS + t); };
+  auto p_hi = [&](int t) { return bar(5 + 2 * kS + t); };
+  auto o_full = [&](int t) { return bar(7 + 2 * kS + t); };
+  const uint32_t mma_done = bar(9 + 2 * kS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10 + 2 * kS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+#ifdef ATTN_TRACE
+  const bool tr = static_cast<int>(blockIdx.x) == g_attn_trace_cta;
+#else
+  const bool tr = false;
+#endif
+  (void)tr;
 
   // ---- tile coordinates
   int bh, pair;
@@ -161,7 +218,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), 128);
+      mbar_init(p_lo(t), 4);  // one arrival per softmax warp
+      mbar_init(p_hi(t), 4);
       mbar_init(o_full(t), 1);
     }
     mbar_init(mma_done, 1);
@@ -179,90 +237,110 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 
   if (warp == 8) {
     // ================================================================ TMA producer
+    // The whole warp runs this loop; one elected lane issues each copy.
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(q_full, C::kQBytes);
-      for (int t = 0; t < 2; ++t) {
-        // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
-        // its results are never stored.
-        const int y = (2 * pair + t) * 128 < N ? (2 * pair + t) * 128 : 0;
-        for (int b = 0; b < C::kBlocks; ++b)
-          tma_load_3d(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y, bh);
-      }
-      int issued = 0;
-      for (int it = 0; it < 2 * n_kv; ++it) {
-        const int j = it >> 1;
-        const int s = it % kS;
-        const uint32_t ph = (it / kS) & 1;
-        if (!mbar_wait(slot_empty(s), ph ^ 1u, p.status, lim)) break;
-        mbar_arrive_expect_tx(slot_full(s), C::kTileBytes);
-        const CUtensorMap* map = (it & 1) ? &p.tm_v : &p.tm_k;
-        for (int b = 0; b < C::kBlocks; ++b)
-          tma_load_3d(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
-                      j * 128, bh);
-        ++issued;
-      }
-      // Drain: every copy this thread issued has landed before the CTA may exit.
-      mbar_wait(q_full, 0, p.status, lim);
-      for (int it = max(0, issued - kS); it < issued; ++it)
-        mbar_wait(slot_full(it % kS), (it / kS) & 1, p.status, lim);
     }
+    __syncwarp();
+    mbar_arrive_expect_tx_elect(q_full, C::kQBytes);
+    for (int t = 0; t < 2; ++t) {
+      // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
+      // its results are never stored.
+      const int y = (2 * pair + t) * 128 < N ? (2 * pair + t) * 128 : 0;
+      for (int b = 0; b < C::kBlocks; ++b)
+        tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y, bh);
+    }
+    int issued = 0;
+    for (int it = 0; it < 2 * n_kv; ++it) {
+      const int j = it >> 1;
+      const int s = it % kS;
+      const uint32_t ph = (it / kS) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ph ^ 1u, p.status, lim))) break;
+      ATTN_TRACE_EV(tr && lane == 0, 5, j, it & 1);
+      mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
+      const CUtensorMap* map = (it & 1) ? &p.tm_v : &p.tm_k;
+      for (int b = 0; b < C::kBlocks; ++b)
+        tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
+                          j * 128, bh);
+      ++issued;
+    }
+    // Drain: every copy this warp issued has landed before the CTA may exit.
+    mbar_wait(q_full, 0, p.status, lim);
+    for (int it = max(0, issued - kS); it < issued; ++it)
+      mbar_wait(slot_full(it % kS), (it / kS) & 1, p.status, lim);
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, p.status, lim);
-      int it = 0;  // ring position of the next K/V tile
-      // S_t = Q_t K_0^T for both tiles
-      if (ok) ok = mbar_wait(slot_full(0), 0, p.status, lim);
-      if (ok) {
-        tc_fence_after();
-        const uint32_t kb = slot_base;
-        issue_qk<C>(tmem + 0, q_base, kb);
-        mma_commit(s_full(0));
-        issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
-        mma_commit(s_full(1));
-        mma_commit(slot_empty(0));
-        it = 1;
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int sv = it % kS;
-        ok = mbar_wait(slot_full(sv), (it / kS) & 1, p.status, lim);
-        if (!ok) break;
-        const int itk = it + 1;
-        const int sk = itk % kS;
-        const bool next = (j + 1 < n_kv);
-        bool k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int kv_end = t ? kv_end1 : kv_end0;
-          if (j < kv_end) {
-            ok = mbar_wait(p_full(t), j & 1, p.status, lim);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv<C>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, slot_base + sv * C::kTileBytes, j > 0);
-            mma_commit(o_full(t));
-          }
-          if (t == 1) mma_commit(slot_empty(sv));
-          if (j + 1 < kv_end) {
-            if (!k_ready) {
-              ok = mbar_wait(slot_full(sk), (itk / kS) & 1, p.status, lim);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
-            mma_commit(s_full(t));
-          }
-        }
-        if (!ok) break;
-        if (next) mma_commit(slot_empty(sk));
-        it += 2;
-      }
-      // Every MMA issued by this thread has completed before TMEM is freed.
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, p.status, lim);
+    // Order per key tile j: for each query tile t, O_t += P_t V_j in two halves
+    // (each half as soon as the softmax has written it), then S_t = Q_t K_{j+1}^T
+    // into the same TMEM columns (tcgen05.mma issued by one thread executes in
+    // order, so the P_t reads precede the S_t overwrite).  The whole warp runs
+    // the loop; one elected lane issues every tcgen05 instruction.
+    auto wait_all = [&](uint32_t b, uint32_t par) {
+      return __all_sync(0xffffffffu, mbar_wait(b, par, p.status, lim));
+    };
+    bool ok = wait_all(q_full, 0);
+    int it = 0;  // ring position of the next K/V tile
+    if (ok) ok = wait_all(slot_full(0), 0);
+    if (ok) {
+      tc_fence_after();
+      issue_qk<C>(tmem + 0, q_base, slot_base);
+      mma_commit_elect(s_full(0));
+      issue_qk<C>(tmem + 128, q_base + C::kTileBytes, slot_base);
+      mma_commit_elect(s_full(1));
+      mma_commit_elect(slot_empty(0));
+      it = 1;
     }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int sv = it % kS;
+      ok = wait_all(slot_full(sv), (it / kS) & 1);
+      if (!ok) break;
+      ATTN_TRACE_EV(tr && lane == 0, 2, j, 4);
+      const int itk = it + 1;
+      const int sk = itk % kS;
+      const bool next = (j + 1 < n_kv);
+      bool k_ready = false;
+      const uint32_t v_addr = slot_base + sv * C::kTileBytes;
+      for (int t = 0; t < 2 && ok; ++t) {
+        const int kv_end = t ? kv_end1 : kv_end0;
+        if (j < kv_end) {
+          ok = wait_all(p_lo(t), j & 1);
+          if (!ok) break;
+          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 0);
+          tc_fence_after();
+          issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
+          ok = wait_all(p_hi(t), j & 1);
+          if (!ok) break;
+          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 1);
+          tc_fence_after();
+          issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
+          // O_t is only read after its last P.V; earlier rescales rely on S_{j+1}
+          // completing after P_j V_j instead.
+          if (j == kv_end - 1) mma_commit_elect(o_full(t));
+          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 2);
+        }
+        if (t == 1) mma_commit_elect(slot_empty(sv));
+        if (j + 1 < kv_end) {
+          if (!k_ready) {
+            ok = wait_all(slot_full(sk), (itk / kS) & 1);
+            if (!ok) break;
+            ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 5);
+            tc_fence_after();
+            k_ready = true;
+          }
+          issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
+          mma_commit_elect(s_full(t));
+          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 3);
+        }
+      }
+      if (!ok) break;
+      if (next) mma_commit_elect(slot_empty(sk));
+      it += 2;
+    }
+    // Every MMA issued by this warp has completed before TMEM is freed.
+    mma_commit_elect(mma_done);
+    mbar_wait(mma_done, 0, p.status, lim);
   } else {
     // ================================================================ softmax warpgroups
     const int t = tid >> 7;                      // query tile of this warpgroup
@@ -274,16 +352,22 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
     const int row = qt * 128 + r;
     const int kv_end = t ? kv_end1 : kv_end0;
     const float sl2 = p.scale_log2;
-    float m2 = -INFINITY;  // running max of s * sl2 (log2 domain)
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    float m2 = -INFINITY;  // reference max of s * sl2 (log2 domain)
     float l = 0.f;         // running sum of p * 2^kPExp
     bool ok = true;
+    const bool trw = tr && r == 0;
+    (void)trw;
 
     for (int j = 0; j < kv_end; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, p.status, lim));
       if (!ok) break;
+      ATTN_TRACE_EV(trw, t, j, 0);
+      ATTN_TRACE_EV(tr && lane == 0, 4, j, t * 4 + (warp & 3));
       tc_fence_after();
       uint32_t u[128];
       tmem_ld128_sync(t_s, u);
+      ATTN_TRACE_EV(tr && lane == 0, 6, j, t * 4 + (warp & 3));
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
@@ -315,59 +399,46 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       const float m_new = (m_cand > m2 + C::kTau) ? m_cand : m2;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m2 - m_use);
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
-      uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
+      ATTN_TRACE_EV(trw, t, j, 1);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds the sum up to key tile j-1 at the old reference: rescale it.
+        // S_j being complete implies O += P_{j-1} V_{j-1} is complete (the MMAs
+        // of one thread complete in issue order and S_j was committed later).
+        // 32 columns at a time: the 128 scores of this row are still live.
+        const uint64_t ax2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32_sync(t_o + c0, o);
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2);
-        const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negx2);
-        s[c] = ex2_approx(f2_lo(a));
-        s[c + 1] = ex2_approx(f2_hi(a));
-        s[c + 2] = ex2_approx(f2_lo(b));
-        s[c + 3] = ex2_approx(f2_hi(b));
-        rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
-        rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
-      }
-      const uint64_t rs = f2_add(rs0, rs1);
-      l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
-      // P goes over the S columns this thread has already consumed.
-      if constexpr (C::kIsFp8) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
-        tmem_st32_sync(t_s, pk);
-      } else {
-        uint32_t pk[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-        tmem_st64_sync(t_s, pk);
-      }
-      if (j > 0) {
-        // O still holds the sum up to key tile j-1 at the old max: rescale by alpha.
-        ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), (j - 1) & 1, p.status, lim));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t o[C::D];
-          tmem_ld_cols<C::D>(t_o, o);
-          const uint64_t ax2 = f2_pack(alpha, alpha);
-#pragma unroll
-          for (int i = 0; i < C::D; i += 2) {
+          for (int i = 0; i < 32; i += 2) {
             const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2);
             o[i] = static_cast<uint32_t>(v);
             o[i + 1] = static_cast<uint32_t>(v >> 32);
           }
-          tmem_st_cols<C::D>(t_o, o);
+          tmem_st32_sync(t_o + c0, o);
         }
       }
+      const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
+      uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
+      softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
       tc_fence_before();
-      mbar_arrive(p_full(t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_lo(t));
+      ATTN_TRACE_EV(trw, t, j, 2);
+      ATTN_TRACE_EV(tr && lane == 0, 7, j, t * 4 + (warp & 3));
+      softmax_half<C, 1>(s, sl2x2, negx2, rs0, rs1, t_s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_hi(t));
+      ATTN_TRACE_EV(trw, t, j, 3);
+      const uint64_t rs = f2_add(rs0, rs1);
+      l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
       m2 = m_new;
     }
 
     if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), (kv_end - 1) & 1, p.status, lim));
+      ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), 0, p.status, lim));  // one phase per CTA
     }
     if (ok) {
       tc_fence_after();
