@@ -56,6 +56,26 @@ int status_ptr(int** out) {
   return ATTN_OK;
 }
 
+// Number of SMs of the current device (looked up once per device).
+int num_sms(int* out) {
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDev) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
+    cache[dev] = n;
+  }
+  *out = cache[dev];
+  return ATTN_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -132,7 +152,10 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.scale_log2 = scale * kLog2e * qds * kds;
   p.o_scale = vds;
   p.timeout_ns = g_wait_limit_ns;
-  cudaError_t e = fp8 ? attn::launch_tc_e4m3(p, d, causal != 0, stream) : attn::launch_tc_bf16(p, d, causal != 0, stream);
+  int sms = 0;
+  if ((st = num_sms(&sms)) != ATTN_OK) return st;
+  cudaError_t e = fp8 ? attn::launch_tc_e4m3(p, d, causal != 0, sms, stream)
+                      : attn::launch_tc_bf16(p, d, causal != 0, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ATTN_OK;
 }

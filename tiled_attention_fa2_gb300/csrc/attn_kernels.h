@@ -40,8 +40,9 @@ struct SimtParams {
 };
 
 // Launchers (defined next to their kernels).  Return the launch error.
-cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, cudaStream_t stream);
-cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, cudaStream_t stream);
+// The tensor-core kernels are persistent: min(#work items, num_sms) CTAs.
+cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
+cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_simt_f32(const SimtParams& p, int d, bool causal, cudaStream_t stream);
 
 }  // namespace attn

@@ -3,9 +3,9 @@
 
 namespace attn {
 
-cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, cudaStream_t stream) {
-  if (d == 128) return causal ? launch_tc<TcCfg<false, 128, true>>(p, stream) : launch_tc<TcCfg<false, 128, false>>(p, stream);
-  if (d == 64) return causal ? launch_tc<TcCfg<false, 64, true>>(p, stream) : launch_tc<TcCfg<false, 64, false>>(p, stream);
+cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream) {
+  if (d == 128) return causal ? launch_tc<TcCfg<false, 128, true>>(p, num_sms, stream) : launch_tc<TcCfg<false, 128, false>>(p, num_sms, stream);
+  if (d == 64) return causal ? launch_tc<TcCfg<false, 64, true>>(p, num_sms, stream) : launch_tc<TcCfg<false, 64, false>>(p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -16,5 +16,8 @@ cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, cudaStream_t s
 extern "C" int attn_trace_bf16(unsigned long long* host, int cta) {
   if (cta >= 0) return static_cast<int>(cudaMemcpyToSymbol(attn::g_attn_trace_cta, &cta, sizeof(int)));
   return static_cast<int>(cudaMemcpyFromSymbol(host, attn::g_attn_trace, sizeof(attn::g_attn_trace)));
+}
+extern "C" int attn_trace_spans_bf16(unsigned long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, attn::g_attn_cta_span, sizeof(attn::g_attn_cta_span)));
 }
 #endif

@@ -3,8 +3,8 @@
 
 namespace attn {
 
-cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, cudaStream_t stream) {
-  if (d == 128) return causal ? launch_tc<TcCfg<true, 128, true>>(p, stream) : launch_tc<TcCfg<true, 128, false>>(p, stream);
+cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream) {
+  if (d == 128) return causal ? launch_tc<TcCfg<true, 128, true>>(p, num_sms, stream) : launch_tc<TcCfg<true, 128, false>>(p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

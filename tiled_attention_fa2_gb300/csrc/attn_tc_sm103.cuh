@@ -59,7 +59,7 @@ struct TcCfg {
   static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, kD, 0, 1);
   static constexpr int kQBytes = 2 * kTileBytes;
-  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 10 barriers + TMEM holder
+  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 13 barriers + TMEM holder
   static constexpr int kSmemBytes = kBarOff + 1024 /*barriers*/ + 1024 /*alignment slack*/;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -147,6 +147,8 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
 #ifdef ATTN_TRACE
 static __device__ unsigned long long g_attn_trace[8 * 64 * 8];
 static __device__ int g_attn_trace_cta = 0;
+// per-CTA [start_ns, end_ns, smid, unused] for occupancy analysis (first 8192 CTAs)
+static __device__ unsigned long long g_attn_cta_span[8192 * 4];
 #define ATTN_TRACE_EV(on, role, j, ev)                                                      \
   do {                                                                                      \
     if ((on) && (j) < 64) g_attn_trace[((role) * 64 + (j)) * 8 + (ev)] = clock64();        \
@@ -156,6 +158,36 @@ static __device__ int g_attn_trace_cta = 0;
   do {                                 \
   } while (0)
 #endif
+
+// Work item -> (b*h, pair of query tiles) and the key tiles each query tile visits.
+struct Item {
+  int bh, pair, kv_end0, kv_end1;
+};
+
+template <class C>
+__device__ __forceinline__ Item decode_item(const TcParams& p, int item, int n_kt) {
+  Item it;
+  if constexpr (C::kCaus) {
+    it.pair = p.n_pairs - 1 - item / p.BH;  // heaviest pairs first
+    it.bh = item % p.BH;
+    it.kv_end0 = min(2 * it.pair + 1, n_kt);
+    it.kv_end1 = min(2 * it.pair + 2, n_kt);
+  } else {
+    it.bh = item / p.n_pairs;  // consecutive items share a head's K/V in L2
+    it.pair = item % p.n_pairs;
+    it.kv_end0 = n_kt;
+    it.kv_end1 = n_kt;
+  }
+  return it;
+}
+
+// Persistent schedule: round r of CTA c takes item r*G + c (even r) or
+// r*G + G-1-c (odd r); with items ordered heaviest first this deals the work
+// out in a snake, so every CTA ends with about the same total.
+__device__ __forceinline__ int item_of_round(int r) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
@@ -167,19 +199,21 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
   const uint32_t q_base = base;
   const uint32_t slot_base = base + C::kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBarOff);
-  // barrier layout: q_full | slot_full[S] | slot_empty[S] | s_full[2] | p_lo[2] | p_hi[2] | o_full[2] | mma_done
+  // q_full | q_empty | slot_full[S] | slot_empty[S] | s_full[2] | p_lo[2] | p_hi[2] | o_full[2] | o_empty[2] | mma_done
   const uint32_t bar0 = smem_u32(bars);
   const int kS = C::kStages;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
   const uint32_t q_full = bar(0);
-  auto slot_full = [&](int s) { return bar(1 + s); };
-  auto slot_empty = [&](int s) { return bar(1 + kS + s); };
-  auto s_full = [&](int t) { return bar(1 + 2 * kS + t); };
-  auto p_lo = [&](int t) { return bar(3 + 2 * kS + t); };
-  auto p_hi = [&](int t) { return bar(5 + 2 * kS + t); };
-  auto o_full = [&](int t) { return bar(7 + 2 * kS + t); };
-  const uint32_t mma_done = bar(9 + 2 * kS);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10 + 2 * kS);
+  const uint32_t q_empty = bar(1);
+  auto slot_full = [&](int s) { return bar(2 + s); };
+  auto slot_empty = [&](int s) { return bar(2 + kS + s); };
+  auto s_full = [&](int t) { return bar(2 + 2 * kS + t); };
+  auto p_lo = [&](int t) { return bar(4 + 2 * kS + t); };
+  auto p_hi = [&](int t) { return bar(6 + 2 * kS + t); };
+  auto o_full = [&](int t) { return bar(8 + 2 * kS + t); };
+  auto o_empty = [&](int t) { return bar(10 + 2 * kS + t); };
+  const uint32_t mma_done = bar(12 + 2 * kS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -191,27 +225,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 #endif
   (void)tr;
 
-  // ---- tile coordinates
-  int bh, pair;
-  if constexpr (C::kCaus) {
-    pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH;  // heaviest query tiles first
-    bh = static_cast<int>(blockIdx.x) % p.BH;
-  } else {
-    bh = static_cast<int>(blockIdx.x) / p.n_pairs;
-    pair = static_cast<int>(blockIdx.x) % p.n_pairs;
-  }
   const int N = p.N;
   const int n_kt = (N + 127) >> 7;
-  int kv_end0 = n_kt, kv_end1 = n_kt;
-  if constexpr (C::kCaus) {
-    kv_end0 = min(2 * pair + 1, n_kt);
-    kv_end1 = min(2 * pair + 2, n_kt);
-  }
-  const int n_kv = kv_end1;  // key tiles visited by the CTA (tile 1 needs >= tile 0)
+  const int total = p.BH * p.n_pairs;
 
   // ---- setup: barriers, TMEM
   if (tid == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kS; ++s) {
       mbar_init(slot_full(s), 1);
       mbar_init(slot_empty(s), 1);
@@ -221,6 +242,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       mbar_init(p_lo(t), 4);  // one arrival per softmax warp
       mbar_init(p_hi(t), 4);
       mbar_init(o_full(t), 1);
+      mbar_init(o_empty(t), 4);
     }
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
@@ -234,42 +256,60 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
   const uint64_t lim = p.timeout_ns;
+#ifdef ATTN_TRACE
+  if (tid == 0 && blockIdx.x < 8192) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_attn_cta_span[blockIdx.x * 4 + 0] = globaltimer_ns();
+    g_attn_cta_span[blockIdx.x * 4 + 2] = smid;
+  }
+#endif
 
   if (warp == 8) {
     // ================================================================ TMA producer
-    // The whole warp runs this loop; one elected lane issues each copy.
+    // The whole warp runs this loop; one elected lane issues each copy.  The
+    // K/V ring position `it` runs on across work items.
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
     }
     __syncwarp();
-    mbar_arrive_expect_tx_elect(q_full, C::kQBytes);
-    for (int t = 0; t < 2; ++t) {
-      // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
-      // its results are never stored.
-      const int y = (2 * pair + t) * 128 < N ? (2 * pair + t) * 128 : 0;
-      for (int b = 0; b < C::kBlocks; ++b)
-        tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y, bh);
-    }
-    int issued = 0;
-    for (int it = 0; it < 2 * n_kv; ++it) {
-      const int j = it >> 1;
-      const int s = it % kS;
-      const uint32_t ph = (it / kS) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ph ^ 1u, p.status, lim))) break;
-      ATTN_TRACE_EV(tr && lane == 0, 5, j, it & 1);
-      mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
-      const CUtensorMap* map = (it & 1) ? &p.tm_v : &p.tm_k;
-      for (int b = 0; b < C::kBlocks; ++b)
-        tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
-                          j * 128, bh);
-      ++issued;
+    int it = 0, nq = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = item_of_round(r);
+      if (item >= total) break;
+      const Item w = decode_item<C>(p, item, n_kt);
+      // Q buffers are free once the previous item's last S = Q K^T completed.
+      if (nq > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty, (nq - 1) & 1, p.status, lim))) break;
+      mbar_arrive_expect_tx_elect(q_full, C::kQBytes);
+      for (int t = 0; t < 2; ++t) {
+        // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
+        // its results are never stored.
+        const int y = (2 * w.pair + t) * 128 < N ? (2 * w.pair + t) * 128 : 0;
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y,
+                            w.bh);
+      }
+      ++nq;
+      for (int k = 0; k < 2 * w.kv_end1; ++k, ++it) {
+        const int j = k >> 1;
+        const int s = it % kS;
+        if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ((it / kS) & 1) ^ 1u, p.status, lim))) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
+        const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
+                            j * 128, w.bh);
+      }
     }
     // Drain: every copy this warp issued has landed before the CTA may exit.
-    mbar_wait(q_full, 0, p.status, lim);
-    for (int it = max(0, issued - kS); it < issued; ++it)
-      mbar_wait(slot_full(it % kS), (it / kS) & 1, p.status, lim);
+    if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, p.status, lim);
+    for (int k = max(0, it - kS); k < it; ++k) mbar_wait(slot_full(k % kS), (k / kS) & 1, p.status, lim);
   } else if (warp == 9) {
     // ================================================================ MMA issuer
     // Order per key tile j: for each query tile t, O_t += P_t V_j in two halves
@@ -280,63 +320,84 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
     auto wait_all = [&](uint32_t b, uint32_t par) {
       return __all_sync(0xffffffffu, mbar_wait(b, par, p.status, lim));
     };
-    bool ok = wait_all(q_full, 0);
-    int it = 0;  // ring position of the next K/V tile
-    if (ok) ok = wait_all(slot_full(0), 0);
-    if (ok) {
+    int it = 0, nq = 0;
+    int np[2] = {0, 0};  // P tiles consumed per query tile (phase of p_lo / p_hi)
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = item_of_round(r);
+      if (item >= total) break;
+      const Item w = decode_item<C>(p, item, n_kt);
+      ok = wait_all(q_full, nq & 1);
+      if (ok) ok = wait_all(slot_full(it % kS), (it / kS) & 1);
+      if (!ok) break;
       tc_fence_after();
-      issue_qk<C>(tmem + 0, q_base, slot_base);
-      mma_commit_elect(s_full(0));
-      issue_qk<C>(tmem + 128, q_base + C::kTileBytes, slot_base);
-      mma_commit_elect(s_full(1));
-      mma_commit_elect(slot_empty(0));
-      it = 1;
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int sv = it % kS;
-      ok = wait_all(slot_full(sv), (it / kS) & 1);
-      if (!ok) break;
-      ATTN_TRACE_EV(tr && lane == 0, 2, j, 4);
-      const int itk = it + 1;
-      const int sk = itk % kS;
-      const bool next = (j + 1 < n_kv);
-      bool k_ready = false;
-      const uint32_t v_addr = slot_base + sv * C::kTileBytes;
-      for (int t = 0; t < 2 && ok; ++t) {
-        const int kv_end = t ? kv_end1 : kv_end0;
-        if (j < kv_end) {
-          ok = wait_all(p_lo(t), j & 1);
-          if (!ok) break;
-          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 0);
-          tc_fence_after();
-          issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
-          ok = wait_all(p_hi(t), j & 1);
-          if (!ok) break;
-          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 1);
-          tc_fence_after();
-          issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
-          // O_t is only read after its last P.V; earlier rescales rely on S_{j+1}
-          // completing after P_j V_j instead.
-          if (j == kv_end - 1) mma_commit_elect(o_full(t));
-          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 2);
-        }
-        if (t == 1) mma_commit_elect(slot_empty(sv));
-        if (j + 1 < kv_end) {
-          if (!k_ready) {
-            ok = wait_all(slot_full(sk), (itk / kS) & 1);
-            if (!ok) break;
-            ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 5);
-            tc_fence_after();
-            k_ready = true;
-          }
-          issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
-          mma_commit_elect(s_full(t));
-          ATTN_TRACE_EV(tr && lane == 0, 2 + t, j, 3);
-        }
+      {
+        const uint32_t kb = slot_base + (it % kS) * C::kTileBytes;
+        issue_qk<C>(tmem + 0, q_base, kb);
+        mma_commit_elect(s_full(0));
+        issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
+        mma_commit_elect(s_full(1));
+        mma_commit_elect(slot_empty(it % kS));
+        if (w.kv_end1 == 1) mma_commit_elect(q_empty);  // that was the item's last use of Q
+        ++it;
       }
-      if (!ok) break;
-      if (next) mma_commit_elect(slot_empty(sk));
-      it += 2;
+      for (int j = 0; ok && j < w.kv_end1; ++j) {
+        const int sv = it % kS;
+        ok = wait_all(slot_full(sv), (it / kS) & 1);
+        if (!ok) break;
+        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2, j, 4);
+        const int itk = it + 1;
+        const int sk = itk % kS;
+        const bool next = (j + 1 < w.kv_end1);
+        bool k_ready = false;
+        const uint32_t v_addr = slot_base + sv * C::kTileBytes;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int kv_end = t ? w.kv_end1 : w.kv_end0;
+          if (j < kv_end) {
+            // The first O_t += P_t V of an item overwrites O_t: the previous
+            // item's epilogue must have read it out.
+            if (j == 0 && nq > 0) {
+              ok = wait_all(o_empty(t), (nq - 1) & 1);
+              if (!ok) break;
+            }
+            ok = wait_all(p_lo(t), np[t] & 1);
+            if (!ok) break;
+            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 0);
+            tc_fence_after();
+            issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
+            ok = wait_all(p_hi(t), np[t] & 1);
+            if (!ok) break;
+            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 1);
+            tc_fence_after();
+            issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
+            ++np[t];
+            // O_t is read only after its last P.V of the item; earlier rescales
+            // rely on S_{j+1} completing after P_j V_j instead.
+            if (j == kv_end - 1) mma_commit_elect(o_full(t));
+            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 2);
+          }
+          if (t == 1) mma_commit_elect(slot_empty(sv));
+          if (j + 1 < kv_end) {
+            if (!k_ready) {
+              ok = wait_all(slot_full(sk), (itk / kS) & 1);
+              if (!ok) break;
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 5);
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
+            mma_commit_elect(s_full(t));
+            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
+          }
+        }
+        if (!ok) break;
+        if (next) {
+          mma_commit_elect(slot_empty(sk));
+          if (j + 2 == w.kv_end1) mma_commit_elect(q_empty);  // the item's last S = Q K^T was just issued
+        }
+        it += next ? 2 : 1;  // V_j, and K_{j+1} if this item has one (the producer loads 2 per key tile)
+      }
+      ++nq;
     }
     // Every MMA issued by this warp has completed before TMEM is freed.
     mma_commit_elect(mma_done);
@@ -348,121 +409,135 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + t * 128;
     const uint32_t t_o = tmem + lane_base + C::kOCol0 + t * C::D;
-    const int qt = 2 * pair + t;
-    const int row = qt * 128 + r;
-    const int kv_end = t ? kv_end1 : kv_end0;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    float m2 = -INFINITY;  // reference max of s * sl2 (log2 domain)
-    float l = 0.f;         // running sum of p * 2^kPExp
-    bool ok = true;
     const bool trw = tr && r == 0;
     (void)trw;
+    int ns = 0, nq = 0;  // S tiles consumed, items finished
+    bool ok = true;
 
-    for (int j = 0; j < kv_end; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, p.status, lim));
-      if (!ok) break;
-      ATTN_TRACE_EV(trw, t, j, 0);
-      ATTN_TRACE_EV(tr && lane == 0, 4, j, t * 4 + (warp & 3));
-      tc_fence_after();
-      uint32_t u[128];
-      tmem_ld128_sync(t_s, u);
-      ATTN_TRACE_EV(tr && lane == 0, 6, j, t * 4 + (warp & 3));
-      float s[128];
+    for (int rr = 0; ok; ++rr) {
+      const int item = item_of_round(rr);
+      if (item >= total) break;
+      const Item w = decode_item<C>(p, item, n_kt);
+      const int qt = 2 * w.pair + t;
+      const int row = qt * 128 + r;
+      const int kv_end = t ? w.kv_end1 : w.kv_end0;
+      float m2 = -INFINITY;  // reference max of s * sl2 (log2 domain)
+      float l = 0.f;         // running sum of p * 2^kPExp
+
+      for (int j = 0; j < kv_end; ++j, ++ns) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), ns & 1, p.status, lim));
+        if (!ok) break;
+        ATTN_TRACE_EV(trw && nq == 0, t, j, 0);
+        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 4, j, t * 4 + (warp & 3));
+        tc_fence_after();
+        uint32_t u[128];
+        tmem_ld128_sync(t_s, u);
+        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 6, j, t * 4 + (warp & 3));
+        float s[128];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
-      const bool diag = C::kCaus && (j == qt);
-      const bool ragged = (j == n_kt - 1) && ((N & 127) != 0);
-      if (diag || ragged) {
-        const int key0 = j * 128;
-        const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+        const bool diag = C::kCaus && (j == qt);
+        const bool ragged = (j == n_kt - 1) && ((N & 127) != 0);
+        if (diag || ragged) {
+          const int key0 = j * 128;
+          const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (key0 + c > lim_key) s[c] = -INFINITY;
-      }
-      // Row max: eight independent three-input max chains, then a short tree.
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-      for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          mx8[i] = fmax3(mx8[i], s[c + i], s[c + i + 1]);
-          mx8[i + 1] = fmax3(mx8[i + 1], s[c + i + 8], s[c + i + 9]);
+          for (int c = 0; c < 128; ++c)
+            if (key0 + c > lim_key) s[c] = -INFINITY;
         }
-      }
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      // Reference max: moves only when the row max grew by more than kTau (then
-      // O and l are rescaled); otherwise p may exceed 1 by at most 2^kTau.
-      const float m_cand = fmaxf(m2, mx * sl2);
-      const float m_new = (m_cand > m2 + C::kTau) ? m_cand : m2;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m2 - m_use);
-      ATTN_TRACE_EV(trw, t, j, 1);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds the sum up to key tile j-1 at the old reference: rescale it.
-        // S_j being complete implies O += P_{j-1} V_{j-1} is complete (the MMAs
-        // of one thread complete in issue order and S_j was committed later).
-        // 32 columns at a time: the 128 scores of this row are still live.
-        const uint64_t ax2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32_sync(t_o + c0, o);
+        // Row max: eight independent three-input max chains, then a short tree.
+        float mx8[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2);
-            o[i] = static_cast<uint32_t>(v);
-            o[i + 1] = static_cast<uint32_t>(v >> 32);
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+        for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            mx8[i] = fmax3(mx8[i], s[c + i], s[c + i + 1]);
+            mx8[i + 1] = fmax3(mx8[i + 1], s[c + i + 8], s[c + i + 9]);
           }
-          tmem_st32_sync(t_o + c0, o);
         }
+        const float mx =
+            fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        // Reference max: moves only when the row max grew by more than kTau (then
+        // O and l are rescaled); otherwise p may exceed 1 by at most 2^kTau.
+        const float m_cand = fmaxf(m2, mx * sl2);
+        const float m_new = (m_cand > m2 + C::kTau) ? m_cand : m2;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m2 - m_use);
+        ATTN_TRACE_EV(trw && nq == 0, t, j, 1);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds the sum up to key tile j-1 at the old reference: rescale it.
+          // S_j being complete implies O += P_{j-1} V_{j-1} is complete (the MMAs
+          // of one thread complete in issue order and S_j was committed later).
+          // 32 columns at a time: the 128 scores of this row are still live.
+          const uint64_t ax2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32_sync(t_o + c0, o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2);
+              o[i] = static_cast<uint32_t>(v);
+              o[i + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            tmem_st32_sync(t_o + c0, o);
+          }
+        }
+        const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
+        uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
+        softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_lo(t));
+        ATTN_TRACE_EV(trw && nq == 0, t, j, 2);
+        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 7, j, t * 4 + (warp & 3));
+        softmax_half<C, 1>(s, sl2x2, negx2, rs0, rs1, t_s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_hi(t));
+        ATTN_TRACE_EV(trw && nq == 0, t, j, 3);
+        const uint64_t rs = f2_add(rs0, rs1);
+        l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
+        m2 = m_new;
       }
-      const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
-      uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
-      softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_lo(t));
-      ATTN_TRACE_EV(trw, t, j, 2);
-      ATTN_TRACE_EV(tr && lane == 0, 7, j, t * 4 + (warp & 3));
-      softmax_half<C, 1>(s, sl2x2, negx2, rs0, rs1, t_s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_hi(t));
-      ATTN_TRACE_EV(trw, t, j, 3);
-      const uint64_t rs = f2_add(rs0, rs1);
-      l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
-      m2 = m_new;
-    }
+      if (!ok) break;
 
-    if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), 0, p.status, lim));  // one phase per CTA
-    }
-    if (ok) {
+      // ---- epilogue of this item: O / l -> bf16, L
+      ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), nq & 1, p.status, lim));
+      if (!ok) break;
       tc_fence_after();
-      const float inv = p.o_scale / l;
-      const bool live = row < N;
       uint32_t o[C::D];
       tmem_ld_cols<C::D>(t_o, o);
-      if (live) {
+      // O is in registers: the next item's first P.V may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty(t));
+      const float inv = p.o_scale / l;
+      if (row < N) {
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                              (static_cast<size_t>(bh) * N + row) * C::D);
+                                              (static_cast<size_t>(w.bh) * N + row) * C::D);
 #pragma unroll
         for (int i = 0; i < C::D / 8; ++i) {
           const float* f = reinterpret_cast<const float*>(o) + 8 * i;
           dst[i] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
                               pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
         }
-        p.lse[static_cast<size_t>(bh) * N + row] = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(w.bh) * N + row] = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       }
+      ++nq;
     }
   }
 
   // ---- teardown
   tc_fence_before();
   __syncthreads();
+#ifdef ATTN_TRACE
+  if (tid == 0 && blockIdx.x < 8192) g_attn_cta_span[blockIdx.x * 4 + 1] = globaltimer_ns();
+#endif
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -470,11 +545,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 }
 
 template <class C>
-cudaError_t launch_tc(const TcParams& p, cudaStream_t stream) {
+cudaError_t launch_tc(const TcParams& p, int num_sms, cudaStream_t stream) {
   auto kern = attn_fwd_tc_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(p.BH) * p.n_pairs;
+  const long long items = static_cast<long long>(p.BH) * p.n_pairs;
+  const long long grid = items < num_sms ? items : num_sms;  // persistent: at most one CTA per SM
   kern<<<dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
