@@ -59,7 +59,7 @@ def call_fwd(lib, **kw):
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(scale=-1.0), 1),
     (dict(causal=2), 1), (dict(dtype=7), 1),
     (dict(d=96), 2), (dict(d=32), 2), (dict(dtype=2, d=64), 2), (dict(dtype=0, d=48), 2),
-    (dict(q=FAKE + 8), 3), (dict(o=FAKE + 4), 3), (dict(lse=FAKE + 2), 3),
+    (dict(q=FAKE + 8), 3), (dict(o=FAKE + 4), 3), (dict(o=FAKE + 16), 3), (dict(lse=FAKE + 2), 3),
     (dict(B=65536, H=65536), 1),
 ])
 def test_invalid_arguments_are_rejected_on_the_host(lib, kw, status):

@@ -132,6 +132,7 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (fp8 ? (d != 128) : (d != 64 && d != 128))
     return fail(ATTN_ERR_UNSUPPORTED, "%s tensor-core path supports d in %s (got %d)", fp8 ? "e4m3" : "bf16",
                 fp8 ? "{128}" : "{64, 128}", d);
+  if (!aligned(o, 32)) return fail(ATTN_ERR_MISALIGNED, "o must be 32-byte aligned for bf16/e4m3 inputs");
   const int BH = B * H;
   const long long n_pairs = (static_cast<long long>(N) + 255) / 256;
   if (n_pairs * BH > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "grid too large (B*H*ceil(N/256))");

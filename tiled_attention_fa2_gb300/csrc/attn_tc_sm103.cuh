@@ -59,7 +59,7 @@ struct TcCfg {
   static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
   static constexpr uint32_t kIdescPV = make_idesc(kFmt, 128, kD, 0, 1);
   static constexpr int kQBytes = 2 * kTileBytes;
-  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 13 barriers + TMEM holder
+  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 15 barriers + TMEM holder
   static constexpr int kSmemBytes = kBarOff + 1024 /*barriers*/ + 1024 /*alignment slack*/;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -145,7 +145,7 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
 // Optional event trace (compile with -DATTN_TRACE): per-CTA cycle stamps of
 // the pipeline hand-offs of one chosen CTA, for timeline analysis.
 #ifdef ATTN_TRACE
-static __device__ unsigned long long g_attn_trace[8 * 64 * 8];
+static __device__ unsigned long long g_attn_trace[9 * 64 * 8];
 static __device__ int g_attn_trace_cta = 0;
 // per-CTA [start_ns, end_ns, smid, unused] for occupancy analysis (first 8192 CTAs)
 static __device__ unsigned long long g_attn_cta_span[8192 * 4];
@@ -199,21 +199,22 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
   const uint32_t q_base = base;
   const uint32_t slot_base = base + C::kQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBarOff);
-  // q_full | q_empty | slot_full[S] | slot_empty[S] | s_full[2] | p_lo[2] | p_hi[2] | o_full[2] | o_empty[2] | mma_done
+  // q_full[2] | q_empty[2] | slot_full[S] | slot_empty[S] | s_full[2] | p_lo[2] | p_hi[2] | o_full[2] |
+  // o_empty[2] | mma_done
   const uint32_t bar0 = smem_u32(bars);
   const int kS = C::kStages;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
-  const uint32_t q_full = bar(0);
-  const uint32_t q_empty = bar(1);
-  auto slot_full = [&](int s) { return bar(2 + s); };
-  auto slot_empty = [&](int s) { return bar(2 + kS + s); };
-  auto s_full = [&](int t) { return bar(2 + 2 * kS + t); };
-  auto p_lo = [&](int t) { return bar(4 + 2 * kS + t); };
-  auto p_hi = [&](int t) { return bar(6 + 2 * kS + t); };
-  auto o_full = [&](int t) { return bar(8 + 2 * kS + t); };
-  auto o_empty = [&](int t) { return bar(10 + 2 * kS + t); };
-  const uint32_t mma_done = bar(12 + 2 * kS);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kS);
+  auto q_full = [&](int t) { return bar(t); };
+  auto q_empty = [&](int t) { return bar(2 + t); };
+  auto slot_full = [&](int s) { return bar(4 + s); };
+  auto slot_empty = [&](int s) { return bar(4 + kS + s); };
+  auto s_full = [&](int t) { return bar(4 + 2 * kS + t); };
+  auto p_lo = [&](int t) { return bar(6 + 2 * kS + t); };
+  auto p_hi = [&](int t) { return bar(8 + 2 * kS + t); };
+  auto o_full = [&](int t) { return bar(10 + 2 * kS + t); };
+  auto o_empty = [&](int t) { return bar(12 + 2 * kS + t); };
+  const uint32_t mma_done = bar(14 + 2 * kS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 15 + 2 * kS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -231,8 +232,10 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 
   // ---- setup: barriers, TMEM
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(q_full(t), 1);
+      mbar_init(q_empty(t), 1);
+    }
     for (int s = 0; s < kS; ++s) {
       mbar_init(slot_full(s), 1);
       mbar_init(slot_empty(s), 1);
@@ -277,38 +280,55 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
     __syncwarp();
     int it = 0, nq = 0;
     bool ok = true;
+    auto load_kv = [&](int k, const Item& w) -> bool {  // ring position `it` <- K_{k/2} (even k) or V_{k/2}
+      const int s = it % kS;
+      if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ((it / kS) & 1) ^ 1u, p.status, lim))) return false;
+      mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
+      const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
+      for (int b = 0; b < C::kBlocks; ++b)
+        tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
+                          (k >> 1) * 128, w.bh);
+      ++it;
+      return true;
+    };
+    auto load_q = [&](int t, const Item& w) -> bool {
+      // Q_t's buffer is free once the previous item's last S_t = Q_t K^T completed.
+      if (nq > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty(t), (nq - 1) & 1, p.status, lim))) return false;
+      // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
+      // its results are never stored.
+      const int y = (2 * w.pair + t) * 128 < N ? (2 * w.pair + t) * 128 : 0;
+      mbar_arrive_expect_tx_elect(q_full(t), C::kTileBytes);
+      for (int b = 0; b < C::kBlocks; ++b)
+        tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full(t), b * C::kBoxCols, y,
+                          w.bh);
+      return true;
+    };
     for (int r = 0; ok; ++r) {
       const int item = item_of_round(r);
       if (item >= total) break;
       const Item w = decode_item<C>(p, item, n_kt);
-      // Q buffers are free once the previous item's last S = Q K^T completed.
-      if (nq > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty, (nq - 1) & 1, p.status, lim))) break;
-      mbar_arrive_expect_tx_elect(q_full, C::kQBytes);
-      for (int t = 0; t < 2; ++t) {
-        // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
-        // its results are never stored.
-        const int y = (2 * w.pair + t) * 128 < N ? (2 * w.pair + t) * 128 : 0;
-        for (int b = 0; b < C::kBlocks; ++b)
-          tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full, b * C::kBoxCols, y,
-                            w.bh);
-      }
+      ATTN_TRACE_EV(tr && lane == 0, 8, r, 0);
+      // Ring order: K_0, V_0, K_1, V_1, ...; Q_0 goes ahead of K_0 and Q_1 ahead of V_0,
+      // so the item's first S_0 = Q_0 K_0^T can start before the previous item's tile 1 is done.
+      ok = load_q(0, w) && load_kv(0, w) && load_q(1, w);
       ++nq;
-      for (int k = 0; k < 2 * w.kv_end1; ++k, ++it) {
-        const int j = k >> 1;
-        const int s = it % kS;
-        if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ((it / kS) & 1) ^ 1u, p.status, lim))) {
-          ok = false;
-          break;
+      // Warm L2 with the next item's Q tiles and first K/V tiles.
+      const int nitem = item_of_round(r + 1);
+      if (ok && nitem < total) {
+        const Item nw = decode_item<C>(p, nitem, n_kt);
+        for (int t = 0; t < 2; ++t) {
+          const int y = (2 * nw.pair + t) * 128 < N ? (2 * nw.pair + t) * 128 : 0;
+          for (int b = 0; b < C::kBlocks; ++b) tma_prefetch_3d_elect(&p.tm_q, b * C::kBoxCols, y, nw.bh);
         }
-        mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
-        const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
-        for (int b = 0; b < C::kBlocks; ++b)
-          tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
-                            j * 128, w.bh);
+        for (int b = 0; b < C::kBlocks; ++b) {
+          tma_prefetch_3d_elect(&p.tm_k, b * C::kBoxCols, 0, nw.bh);
+          tma_prefetch_3d_elect(&p.tm_v, b * C::kBoxCols, 0, nw.bh);
+        }
       }
+      for (int k = 1; ok && k < 2 * w.kv_end1; ++k) ok = load_kv(k, w);
     }
     // Drain: every copy this warp issued has landed before the CTA may exit.
-    if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, p.status, lim);
+    for (int t = 0; nq > 0 && t < 2; ++t) mbar_wait(q_full(t), (nq - 1) & 1, p.status, lim);
     for (int k = max(0, it - kS); k < it; ++k) mbar_wait(slot_full(k % kS), (k / kS) & 1, p.status, lim);
   } else if (warp == 9) {
     // ================================================================ MMA issuer
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       const int item = item_of_round(r);
       if (item >= total) break;
       const Item w = decode_item<C>(p, item, n_kt);
-      ok = wait_all(q_full, nq & 1);
+      ok = wait_all(q_full(0), nq & 1);
       if (ok) ok = wait_all(slot_full(it % kS), (it / kS) & 1);
       if (!ok) break;
       tc_fence_after();
@@ -335,11 +355,16 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         const uint32_t kb = slot_base + (it % kS) * C::kTileBytes;
         issue_qk<C>(tmem + 0, q_base, kb);
         mma_commit_elect(s_full(0));
+        if (w.kv_end0 == 1) mma_commit_elect(q_empty(0));  // the item's last use of Q_0
+        ok = wait_all(q_full(1), nq & 1);
+        if (!ok) break;
+        tc_fence_after();
         issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
         mma_commit_elect(s_full(1));
+        if (w.kv_end1 == 1) mma_commit_elect(q_empty(1));
         mma_commit_elect(slot_empty(it % kS));
-        if (w.kv_end1 == 1) mma_commit_elect(q_empty);  // that was the item's last use of Q
         ++it;
+        ATTN_TRACE_EV(tr && lane == 0, 8, r, 1);
       }
       for (int j = 0; ok && j < w.kv_end1; ++j) {
         const int sv = it % kS;
@@ -387,14 +412,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
             }
             issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
             mma_commit_elect(s_full(t));
+            if (j + 2 == kv_end) mma_commit_elect(q_empty(t));  // the item's last S_t = Q_t K^T
             ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
           }
         }
         if (!ok) break;
-        if (next) {
-          mma_commit_elect(slot_empty(sk));
-          if (j + 2 == w.kv_end1) mma_commit_elect(q_empty);  // the item's last S = Q K^T was just issued
-        }
+        if (next) mma_commit_elect(slot_empty(sk));
         it += next ? 2 : 1;  // V_j, and K_{j+1} if this item has one (the producer loads 2 per key tile)
       }
       ++nq;
@@ -430,6 +453,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), ns & 1, p.status, lim));
         if (!ok) break;
         ATTN_TRACE_EV(trw && nq == 0, t, j, 0);
+        ATTN_TRACE_EV(trw && j == 0, 8, rr, 2 + 3 * t);
         ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 4, j, t * 4 + (warp & 3));
         tc_fence_after();
         uint32_t u[128];
@@ -509,6 +533,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       // ---- epilogue of this item: O / l -> bf16, L
       ok = __all_sync(0xffffffffu, mbar_wait(o_full(t), nq & 1, p.status, lim));
       if (!ok) break;
+      ATTN_TRACE_EV(trw, 8, rr, 3 + 3 * t);
       tc_fence_after();
       uint32_t o[C::D];
       tmem_ld_cols<C::D>(t_o, o);
@@ -518,16 +543,18 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       if (lane == 0) mbar_arrive(o_empty(t));
       const float inv = p.o_scale / l;
       if (row < N) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                              (static_cast<size_t>(w.bh) * N + row) * C::D);
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(w.bh) * N + row) * C::D;
 #pragma unroll
-        for (int i = 0; i < C::D / 8; ++i) {
-          const float* f = reinterpret_cast<const float*>(o) + 8 * i;
-          dst[i] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                              pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+        for (int i = 0; i < C::D / 16; ++i) {
+          const float* f = reinterpret_cast<const float*>(o) + 16 * i;
+          st_global_v8(dst + 16 * i, pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                       pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv),
+                       pack_bf16x2(f[8] * inv, f[9] * inv), pack_bf16x2(f[10] * inv, f[11] * inv),
+                       pack_bf16x2(f[12] * inv, f[13] * inv), pack_bf16x2(f[14] * inv, f[15] * inv));
         }
         p.lse[static_cast<size_t>(w.bh) * N + row] = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       }
+      ATTN_TRACE_EV(trw, 8, rr, 4 + 3 * t);
       ++nq;
     }
   }

@@ -56,6 +56,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Gives up after
 // `limit_ns` of wall-clock time: writes the timeout status and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, uint64_t limit_ns) {
@@ -64,6 +75,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) {
+      atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Same, for waits that are expected to be long (producers waiting for a
+// buffer to drain): sleeps between polls so the waiting warp leaves the issue
+// slots of its sub-partition to the compute warps.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* status, uint64_t limit_ns,
+                                                unsigned sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0u && globaltimer_ns() - t0 > limit_ns) {
       atomicExch(status, kStatusTimeout);
       return false;
     }
@@ -199,6 +227,24 @@ __device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const CUtensorMa
       " [%0], [%1, {%3, %4, %5}], [%2];\n}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// L2 prefetch of one TMA box (no shared memory, no barrier), elected lane.
+__device__ __forceinline__ void tma_prefetch_3d_elect(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// 32-byte global store (sm_100+ vector width).
+__device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a0), "r"(a1), "r"(a2), "r"(a3),
+               "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05 async op issued so far by this thread completes.
