@@ -138,6 +138,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's value (the job ends when the last rank ends)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    dev = device if (device is not None and dist.get_backend() == "nccl") else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s under weak scaling: every rank processes its own batch
+    of the workload, so the work is world * steps * flops_per_step and the
+    time is the slowest rank's."""
+    return flops_per_step * world * steps / (max_ms * 1e-3) / 1e12
+
+
 def make_device_inputs(w: dict, device, seed: int):
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=w["q_mult"])
@@ -217,13 +234,9 @@ def run_gpu_arm(args, w):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
     times_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(times_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), dist, device)
     flops = inputs.attention_flops(B, H, N, d, causal)
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, total_ms)
     mean_ms = total_ms / args.steps
 
     # ---- end to end: pinned host buffers through the C ABI (copies inside the timed region)
@@ -250,11 +263,7 @@ def run_gpu_arm(args, w):
         e2e_call()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, device)
     in_bytes = sum(t.numel() * t.element_size() for t in host)
     out_bytes = o.numel() * o.element_size() + lse.numel() * 4
 
@@ -287,7 +296,7 @@ def run_gpu_arm(args, w):
                      "frac": round(achieved / peak, 4), "peak_source": f"{peaks_src}: {peak_note}",
                      "traffic": profile_traffic(args.workload)},
         "clocks": clocks,
-        "e2e": {"value": round(flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(flops, world, e2e_steps, e2e_ms), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
                 "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes},
         "gpu_launches": args.steps,

@@ -103,6 +103,16 @@ int attn_get_device_status(void* stream);
  * launches from this process; default 2e9 (2 s).  Returns the previous value. */
 uint64_t attn_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Self-test of the bounded device-side wait that every kernel of this library
+ * uses: enqueues one thread that waits on an mbarrier nothing ever signals,
+ * with the given limit (nanoseconds, >= 1e6).  The wait gives up, records
+ * ATTN_ERR_TIMEOUT in the device status word and the kernel returns; a later
+ * attn_get_device_status() reports (and clears) it.  No fault, no trap, and the
+ * device stays usable.  Returns ATTN_OK once enqueued.
+ */
+int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(int status);
 

@@ -38,3 +38,18 @@ def built_library():
     from tiled_attention_fa2_gb300 import _build
 
     return _build.build()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the measured parity errors (ATTN_PARITY_REPORT=path.json)."""
+    path = os.environ.get("ATTN_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from parity import REPORT
+    except ImportError:
+        return
+    import json
+
+    with open(path, "w") as f:
+        json.dump(REPORT, f, indent=1)

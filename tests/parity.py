@@ -100,6 +100,14 @@ def oracle_rows(case: Case, causal: bool, rows: np.ndarray):
     return o, lse
 
 
-def errors(o_gpu, l_gpu, o_ref, l_ref):
+# Measured errors of every compared case, written as JSON at the end of the
+# session when ATTN_PARITY_REPORT names a file (see tests/conftest.py).
+REPORT = []
+
+
+def errors(o_gpu, l_gpu, o_ref, l_ref, label=None):
     assert np.isfinite(o_gpu).all() and np.isfinite(l_gpu).all(), "non-finite GPU output"
-    return float(np.abs(o_gpu - o_ref).max()), float(np.abs(l_gpu - l_ref).max())
+    eo, el = float(np.abs(o_gpu - o_ref).max()), float(np.abs(l_gpu - l_ref).max())
+    if label is not None:
+        REPORT.append({"case": label, "o_max_abs": eo, "l_max_abs": el, "compared": int(o_ref.size)})
+    return eo, el

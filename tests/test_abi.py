@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_fp8", "attn_fwd_host", "attn_get_device_status",
-            "attn_status_string", "attn_last_error", "attn_set_wait_limit_ns"} <= set(names)
+            "attn_status_string", "attn_last_error", "attn_set_wait_limit_ns",
+            "attn_selftest_wait_timeout"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -93,3 +94,7 @@ def test_binding_raises_when_library_is_missing(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(ImportError):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_selftest_limit_is_validated_on_the_host(lib):
+    assert lib.attn_selftest_wait_timeout(999_999, None) == 1

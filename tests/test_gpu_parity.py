@@ -32,7 +32,9 @@ def _check(case, causal, rows=None, tight=None):
         o_ref, l_ref = oracle_rows(case, causal, rows)
         o = np.stack([o[h][rows[h]] for h in range(o.shape[0])])
         l = np.stack([l[h][rows[h]] for h in range(l.shape[0])])
-    eo, el = errors(o, l, o_ref, l_ref)
+    label = getattr(case, "name", "") + f" {case.dtype} B{case.B} H{case.H} N{case.N} d{case.d} causal={int(causal)} " + (
+        "full" if rows is None else f"{rows.shape[1]} rows/head")
+    eo, el = errors(o, l, o_ref, l_ref, label=label)
     assert eo <= TOL_O[case.dtype], f"O max-abs error {eo:.3e}"
     assert el <= TOL_L[case.dtype], f"L max-abs error {el:.3e}"
     if tight is not None:
@@ -78,7 +80,9 @@ def test_many_heads_small_n():
 
 def _wl(name):
     w = inputs.WORKLOADS[name]
-    return make_case(w["B"], w["H"], w["N"], w["d"], w["dtype"], q_mult=w["q_mult"]), w["causal"]
+    case = make_case(w["B"], w["H"], w["N"], w["d"], w["dtype"], q_mult=w["q_mult"])
+    case.name = name
+    return case, w["causal"]
 
 
 def test_tiny_f32_workload():

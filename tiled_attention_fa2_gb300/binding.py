@@ -29,6 +29,7 @@ SIGNATURES = {
     "attn_fwd_host": (_I, [_VP] * 10 + [_I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _VP]),
     "attn_get_device_status": (_I, [_VP]),
     "attn_set_wait_limit_ns": (_U64, [_U64]),
+    "attn_selftest_wait_timeout": (_I, [_U64, _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_error": (ctypes.c_char_p, []),
 }
@@ -160,6 +161,12 @@ def get_device_status(stream=None) -> int:
     """Synchronise and return the device status (0 = ok, 5 = a wait timed out)."""
     lib = load_library()
     return int(lib.attn_get_device_status(_stream_handle(stream, None)))
+
+
+def selftest_wait_timeout(limit_ns: int = 10_000_000, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (see include/attn_fa2.h)."""
+    lib = load_library()
+    _check(lib.attn_selftest_wait_timeout(int(limit_ns), _stream_handle(stream, None)))
 
 
 def set_wait_limit_ns(ns: int) -> int:

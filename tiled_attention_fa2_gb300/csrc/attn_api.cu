@@ -14,6 +14,7 @@
 
 #include "attn_fa2.h"
 #include "attn_kernels.h"
+#include "ptx_sm103.cuh"
 
 namespace {
 
@@ -193,6 +194,18 @@ int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 bool good_descale(float x) { return x > 0.f && std::isfinite(x); }
 
+// One thread waits on an mbarrier that is never signalled; the bounded wait
+// gives up after limit_ns and writes the timeout status.
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    attn::mbar_init(attn::smem_u32(&bar), 1);
+    attn::fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)attn::mbar_wait(attn::smem_u32(&bar), 0, status, limit_ns);
+}
+
 }  // namespace
 
 extern "C" {
@@ -260,6 +273,18 @@ int attn_get_device_status(void* stream) {
       return cuda_fail(e, "clear status");
     return fail(ATTN_ERR_TIMEOUT, "a kernel gave up on a device-side wait");
   }
+  return ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  g_last_error[0] = '\0';
+  if (limit_ns < 1000000ull) return fail(ATTN_ERR_INVALID_ARG, "limit must be >= 1e6 ns");
+  int* status = nullptr;
+  int st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ATTN_OK;
 }
 
