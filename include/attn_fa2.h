@@ -36,6 +36,7 @@
 #ifndef ATTN_FA2_H
 #define ATTN_FA2_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -90,6 +91,34 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
 int attn_fwd_host(const void* h_q, const void* h_k, const void* h_v, void* h_o, float* h_lse, void* d_q,
                   void* d_k, void* d_v, void* d_o, float* d_lse, int B, int H, int N, int d, float scale,
                   float q_descale, float k_descale, float v_descale, int causal, int dtype, void* stream);
+
+/*
+ * Split-KV planning ("Kernels and Memory in LLM Inference", Flash-Decoding:
+ * split the keys into chunks processed in parallel, then merge the partial
+ * results by a log-sum-exp rescale).  For the given sizes and requested split
+ * count (0 = enough work items to fill every SM of the current device; the
+ * count never exceeds the number of 128-key tiles and no key range is left
+ * empty) writes the resolved count to *splits_out and the workspace size
+ * attn_fwd_split needs to *workspace_bytes_out (0 when it resolves to 1).
+ * Either output pointer may be NULL.  d in {64, 128}.
+ */
+int attn_fwd_split_plan(int B, int H, int N, int d, int n_splits, int* splits_out, size_t* workspace_bytes_out);
+
+/*
+ * Non-causal forward with the keys split into ranges (see attn_fwd_split_plan):
+ * each (query tile pair, key range) is a separate work item, which keeps every
+ * SM busy when B*H*ceil(N/256) is small.  Each range writes its normalised O
+ * (fp32) and its L into `workspace`, then a merge kernel writes o (bf16) and
+ * lse (fp32) exactly as attn_fwd would.
+ *   dtype     : ATTN_BF16 (descales ignored) or ATTN_E4M3 (per-tensor descales).
+ *   causal    : must be 0 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   workspace : device, 256-byte aligned, >= the planned bytes, owned by the
+ *               caller; its contents are scratch (overwritten by every call).
+ * With one resolved range it runs attn_fwd's kernel and touches no workspace.
+ */
+int attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, float q_descale, float k_descale, float v_descale, int causal, int dtype,
+                   int n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

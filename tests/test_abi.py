@@ -98,3 +98,41 @@ def test_binding_raises_when_library_is_missing(tmp_path, monkeypatch):
 
 def test_selftest_limit_is_validated_on_the_host(lib):
     assert lib.attn_selftest_wait_timeout(999_999, None) == 1
+
+
+def test_split_plan_arithmetic(lib):
+    import ctypes
+    s = ctypes.c_int(0)
+    nb = ctypes.c_size_t(0)
+    # N = 1000 -> 8 key tiles; 3 requested -> 3 tiles per range -> 3 ranges
+    assert lib.attn_fwd_split_plan(1, 2, 1000, 128, 3, ctypes.byref(s), ctypes.byref(nb)) == 0
+    assert s.value == 3
+    rows = 1 * 2 * 1000
+    o_bytes = (3 * rows * 128 * 4 + 255) // 256 * 256
+    assert nb.value == o_bytes + 3 * rows * 4
+    # 6 requested over 8 tiles -> 2 tiles per range -> 4 ranges (no empty range)
+    assert lib.attn_fwd_split_plan(1, 2, 1000, 128, 6, ctypes.byref(s), None) == 0
+    assert s.value == 4
+    # never more ranges than key tiles; one range needs no workspace
+    assert lib.attn_fwd_split_plan(1, 1, 100, 64, 9, ctypes.byref(s), ctypes.byref(nb)) == 0
+    assert s.value == 1 and nb.value == 0
+    assert lib.attn_fwd_split_plan(0, 1, 100, 64, 2, None, None) == 1
+    assert lib.attn_fwd_split_plan(1, 1, 100, 96, 2, None, None) == 1  # d must be 64 or 128
+    assert lib.attn_fwd_split_plan(1, 1, 100, 64, -1, None, None) == 1
+
+
+def call_split(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=1000, d=128, scale=0.1, qd=1.0, kd=1.0, vd=1.0,
+             causal=0, dtype=1, n_splits=4, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return lib.attn_fwd_split(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"], a["scale"],
+                              a["qd"], a["kd"], a["vd"], a["causal"], a["dtype"], a["n_splits"], a["ws"], a["wsb"],
+                              None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(causal=1), 2), (dict(dtype=0, d=64), 2), (dict(ws=None), 1), (dict(wsb=1024), 1),
+    (dict(ws=FAKE + 16), 3), (dict(dtype=2, qd=0.0), 1), (dict(n_splits=-2), 1), (dict(q=None), 1),
+])
+def test_split_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert call_split(lib, **kw) == status

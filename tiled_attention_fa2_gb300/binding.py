@@ -30,6 +30,9 @@ SIGNATURES = {
     "attn_get_device_status": (_I, [_VP]),
     "attn_set_wait_limit_ns": (_U64, [_U64]),
     "attn_selftest_wait_timeout": (_I, [_U64, _VP]),
+    "attn_fwd_split_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
+    "attn_fwd_split": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _I, _VP, ctypes.c_size_t,
+                            _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_error": (ctypes.c_char_p, []),
 }
@@ -155,6 +158,34 @@ def attn_fwd_host(h_q, h_k, h_v, h_o, h_lse, d_q, d_k, d_v, d_o, d_lse, scale=No
                              d_q.data_ptr(), d_k.data_ptr(), d_v.data_ptr(), d_o.data_ptr(), d_lse.data_ptr(),
                              B, H, N, d, scale, float(descales[0]), float(descales[1]), float(descales[2]),
                              int(bool(causal)), code, _stream_handle(stream, d_q.device)))
+
+
+def split_plan(B, H, N, d, n_splits=0):
+    """(resolved split count, workspace bytes) of attn_fwd_split for these sizes."""
+    lib = load_library()
+    s = ctypes.c_int(0)
+    nb = ctypes.c_size_t(0)
+    _check(lib.attn_fwd_split_plan(int(B), int(H), int(N), int(d), int(n_splits), ctypes.byref(s), ctypes.byref(nb)))
+    return s.value, nb.value
+
+
+def attn_fwd_split(q, k, v, n_splits=0, descales=None, o=None, lse=None, scale=None, workspace=None, stream=None):
+    """Non-causal split-KV forward (bf16, or e4m3 codes with `descales`).
+    Allocates the workspace with torch unless one is given.  Returns (o, lse)."""
+    B, H, N, d = _shape(q, k, v)
+    code = _dtype_code(q)
+    o, lse = _outputs(q, o, lse, B, H, N, d, code)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _, nbytes = split_plan(B, H, N, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    ds = descales if descales is not None else (1.0, 1.0, 1.0)
+    lib = load_library()
+    _check(lib.attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              scale, float(ds[0]), float(ds[1]), float(ds[2]), 0, code, int(n_splits),
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream, q.device)))
+    return o, lse
 
 
 def get_device_status(stream=None) -> int:

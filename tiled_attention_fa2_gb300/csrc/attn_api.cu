@@ -128,8 +128,40 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Split-KV plan: the number of key ranges (resolved from `req`, 0 = enough
+// work items to fill every SM), the key tiles per range, and the workspace bytes.
+struct SplitPlan {
+  int splits, kt_per;
+  size_t ws_bytes, part_l_offset;
+};
+
+int plan_split(int B, int H, int N, int d, int req, SplitPlan* out) {
+  if (req < 0) return fail(ATTN_ERR_INVALID_ARG, "n_splits must be >= 0 (got %d)", req);
+  const long long n_kt = (static_cast<long long>(N) + 127) / 128;
+  const long long items = static_cast<long long>(B) * H * ((static_cast<long long>(N) + 255) / 256);
+  long long s = req;
+  if (s == 0) {
+    int sms = 0;
+    int st = num_sms(&sms);
+    if (st != ATTN_OK) return st;
+    s = items >= sms ? 1 : (sms + items - 1) / items;
+  }
+  if (s > n_kt) s = n_kt;
+  if (s < 1) s = 1;
+  const long long kt_per = (n_kt + s - 1) / s;
+  s = (n_kt + kt_per - 1) / kt_per;  // no empty key range
+  out->splits = static_cast<int>(s);
+  out->kt_per = static_cast<int>(kt_per);
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t o_bytes = (s * rows * static_cast<size_t>(d) * 4 + 255) / 256 * 256;
+  out->part_l_offset = o_bytes;
+  out->ws_bytes = s == 1 ? 0 : o_bytes + s * rows * 4;
+  return ATTN_OK;
+}
+
 int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-           float scale, float qds, float kds, float vds, int causal, bool fp8, cudaStream_t stream) {
+           float scale, float qds, float kds, float vds, int causal, bool fp8, cudaStream_t stream,
+           int n_splits = 1, int kt_per = 0, float* part_o = nullptr, float* part_l = nullptr) {
   if (fp8 ? (d != 128) : (d != 64 && d != 128))
     return fail(ATTN_ERR_UNSUPPORTED, "%s tensor-core path supports d in %s (got %d)", fp8 ? "e4m3" : "bf16",
                 fp8 ? "{128}" : "{64, 128}", d);
@@ -154,6 +186,11 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.scale_log2 = scale * kLog2e * qds * kds;
   p.o_scale = vds;
   p.timeout_ns = g_wait_limit_ns;
+  p.n_splits = n_splits;
+  p.kt_per_split = n_splits == 1 ? (N + 127) / 128 : kt_per;
+  p.part_o = part_o;
+  p.part_l = part_l;
+  if (n_pairs * BH * n_splits > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many work items");
   int sms = 0;
   if ((st = num_sms(&sms)) != ATTN_OK) return st;
   cudaError_t e = fp8 ? attn::launch_tc_e4m3(p, d, causal != 0, sms, stream)
@@ -285,6 +322,57 @@ int attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ATTN_OK;
+}
+
+int attn_fwd_split_plan(int B, int H, int N, int d, int n_splits, int* splits_out, size_t* workspace_bytes_out) {
+  g_last_error[0] = '\0';
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128))
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must be >= 1 and d in {64, 128}");
+  SplitPlan plan;
+  int st = plan_split(B, H, N, d, n_splits, &plan);
+  if (st != ATTN_OK) return st;
+  if (splits_out) *splits_out = plan.splits;
+  if (workspace_bytes_out) *workspace_bytes_out = plan.ws_bytes;
+  return ATTN_OK;
+}
+
+int attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, float q_descale, float k_descale, float v_descale, int causal, int dtype,
+                   int n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_common(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (dtype != ATTN_BF16 && dtype != ATTN_E4M3)
+    return fail(ATTN_ERR_UNSUPPORTED, "split-KV runs on the tensor-core paths (bf16, e4m3) only");
+  if (causal) return fail(ATTN_ERR_UNSUPPORTED, "split-KV is implemented for non-causal attention only");
+  const bool fp8 = dtype == ATTN_E4M3;
+  if (fp8 && (!good_descale(q_descale) || !good_descale(k_descale) || !good_descale(v_descale)))
+    return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
+  SplitPlan plan;
+  if ((st = plan_split(B, H, N, d, n_splits, &plan)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float qds = fp8 ? q_descale : 1.f, kds = fp8 ? k_descale : 1.f, vds = fp8 ? v_descale : 1.f;
+  if (plan.splits == 1) return run_tc(q, k, v, o, lse, B, H, N, d, scale, qds, kds, vds, 0, fp8, s);
+  if (static_cast<long long>(B) * H * N > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "B*H*N too large for split-KV");
+  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is null (%zu bytes needed)", plan.ws_bytes);
+  if (workspace_bytes < plan.ws_bytes)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
+                plan.ws_bytes);
+  if (!aligned(workspace, 256)) return fail(ATTN_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  float* part_o = static_cast<float*>(workspace);
+  float* part_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.part_l_offset);
+  st = run_tc(q, k, v, o, lse, B, H, N, d, scale, qds, kds, vds, 0, fp8, s, plan.splits, plan.kt_per, part_o, part_l);
+  if (st != ATTN_OK) return st;
+  attn::CombineParams cp;
+  cp.part_o = part_o;
+  cp.part_l = part_l;
+  cp.o = o;
+  cp.lse = lse;
+  cp.rows = B * H * N;
+  cp.n_splits = plan.splits;
+  cudaError_t e = attn::launch_split_combine(cp, d, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return ATTN_OK;
 }
 

@@ -23,8 +23,27 @@ struct TcParams {
   int N;                // sequence length (queries = keys)
   int n_pairs;          // ceil(N / 256): CTAs per head (two 128-row query tiles each)
   float scale_log2;     // softmax scale * log2(e) * q_descale * k_descale
-  float o_scale;        // v_descale / P multiplier (1 for bf16, v_descale/256 for e4m3)
+  float o_scale;        // multiplies O after the division by l (v_descale for e4m3, 1 for bf16)
   unsigned long long timeout_ns;
+  // Split-KV (non-causal only): the key tiles are cut into n_splits ranges of
+  // kt_per_split tiles; each (query tile pair, range) is a separate work item
+  // whose normalised O (fp32) and L go to part_o [n_splits, BH, N, d] and
+  // part_l [n_splits, BH, N].  n_splits == 1 and part_o == nullptr: O and L are
+  // written directly.
+  int n_splits;
+  int kt_per_split;
+  float* part_o;
+  float* part_l;
+};
+
+// Arguments of the split-KV combine kernel.
+struct CombineParams {
+  const float* part_o;  // [n_splits, rows, d]
+  const float* part_l;  // [n_splits, rows]
+  void* o;              // bf16 [rows, d]
+  float* lse;           // fp32 [rows]
+  int rows;             // B * H * N
+  int n_splits;
 };
 
 // Arguments of the SIMT fp32 forward kernel.
@@ -44,5 +63,6 @@ struct SimtParams {
 cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_simt_f32(const SimtParams& p, int d, bool causal, cudaStream_t stream);
+cudaError_t launch_split_combine(const CombineParams& p, int d, cudaStream_t stream);
 
 }  // namespace attn

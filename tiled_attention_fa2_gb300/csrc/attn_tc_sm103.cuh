@@ -165,7 +165,9 @@ static __device__ unsigned long long g_attn_cta_span[8192 * 4];
 
 // Work item -> (b*h, pair of query tiles) and the key tiles each query tile visits.
 struct Item {
-  int bh, pair, kv_end0, kv_end1;
+  int bh, pair, split;
+  int kv0;               // first key tile of the item's range
+  int kv_end0, kv_end1;  // key tiles visited by query tile 0 / 1 (counted from kv0)
 };
 
 template <class C>
@@ -174,13 +176,21 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int item, int n_k
   if constexpr (C::kCaus) {
     it.pair = p.n_pairs - 1 - item / p.BH;  // heaviest pairs first
     it.bh = item % p.BH;
+    it.split = 0;
+    it.kv0 = 0;
     it.kv_end0 = min(2 * it.pair + 1, n_kt);
     it.kv_end1 = min(2 * it.pair + 2, n_kt);
   } else {
-    it.bh = item / p.n_pairs;  // consecutive items share a head's K/V in L2
-    it.pair = item % p.n_pairs;
-    it.kv_end0 = n_kt;
-    it.kv_end1 = n_kt;
+    // (b*h, key range, query pair), fastest last: consecutive items share the
+    // same head and key range, so concurrent CTAs reuse those K/V tiles in L2.
+    const int per_bh = p.n_pairs * p.n_splits;
+    it.bh = item / per_bh;
+    const int rem = item % per_bh;
+    it.split = rem / p.n_pairs;
+    it.pair = rem % p.n_pairs;
+    it.kv0 = it.split * p.kt_per_split;
+    it.kv_end0 = min(n_kt - it.kv0, p.kt_per_split);
+    it.kv_end1 = it.kv_end0;
   }
   return it;
 }
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 
   const int N = p.N;
   const int n_kt = (N + 127) >> 7;
-  const int total = p.BH * p.n_pairs;
+  const int total = p.BH * p.n_pairs * p.n_splits;
 
   // ---- setup: barriers, TMEM
   if (tid == 0) {
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
       for (int b = 0; b < C::kBlocks; ++b)
         tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
-                          (k >> 1) * 128, w.bh);
+                          (w.kv0 + (k >> 1)) * 128, w.bh);
       ++it;
       return true;
     };
@@ -325,8 +335,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
           for (int b = 0; b < C::kBlocks; ++b) tma_prefetch_3d_elect(&p.tm_q, b * C::kBoxCols, y, nw.bh);
         }
         for (int b = 0; b < C::kBlocks; ++b) {
-          tma_prefetch_3d_elect(&p.tm_k, b * C::kBoxCols, 0, nw.bh);
-          tma_prefetch_3d_elect(&p.tm_v, b * C::kBoxCols, 0, nw.bh);
+          tma_prefetch_3d_elect(&p.tm_k, b * C::kBoxCols, nw.kv0 * 128, nw.bh);
+          tma_prefetch_3d_elect(&p.tm_v, b * C::kBoxCols, nw.kv0 * 128, nw.bh);
         }
       }
       for (int k = 1; ok && k < 2 * w.kv_end1; ++k) ok = load_kv(k, w);
@@ -466,10 +476,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
-        const bool diag = C::kCaus && (j == qt);
-        const bool ragged = (j == n_kt - 1) && ((N & 127) != 0);
+        const int jj = w.kv0 + j;  // absolute key tile
+        const bool diag = C::kCaus && (jj == qt);
+        const bool ragged = (jj == n_kt - 1) && ((N & 127) != 0);
         if (diag || ragged) {
-          const int key0 = j * 128;
+          const int key0 = jj * 128;
           const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -546,17 +557,33 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty(t));
       const float inv = p.o_scale / l;
+      const float lse_v = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       if (row < N) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(w.bh) * N + row) * C::D;
+        if (p.part_o != nullptr) {
+          // Split-KV: this key range's normalised O (fp32) and L, merged later.
+          const size_t prow = (static_cast<size_t>(w.split) * p.BH + w.bh) * N + row;
+          float* dst = p.part_o + prow * C::D;
 #pragma unroll
-        for (int i = 0; i < C::D / 16; ++i) {
-          const float* f = reinterpret_cast<const float*>(o) + 16 * i;
-          st_global_v8(dst + 16 * i, pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                       pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv),
-                       pack_bf16x2(f[8] * inv, f[9] * inv), pack_bf16x2(f[10] * inv, f[11] * inv),
-                       pack_bf16x2(f[12] * inv, f[13] * inv), pack_bf16x2(f[14] * inv, f[15] * inv));
+          for (int i = 0; i < C::D / 8; ++i) {
+            const float* f = reinterpret_cast<const float*>(o) + 8 * i;
+            st_global_v8(dst + 8 * i, __float_as_uint(f[0] * inv), __float_as_uint(f[1] * inv),
+                         __float_as_uint(f[2] * inv), __float_as_uint(f[3] * inv), __float_as_uint(f[4] * inv),
+                         __float_as_uint(f[5] * inv), __float_as_uint(f[6] * inv), __float_as_uint(f[7] * inv));
+          }
+          p.part_l[prow] = lse_v;
+        } else {
+          __nv_bfloat16* dst =
+              reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(w.bh) * N + row) * C::D;
+#pragma unroll
+          for (int i = 0; i < C::D / 16; ++i) {
+            const float* f = reinterpret_cast<const float*>(o) + 16 * i;
+            st_global_v8(dst + 16 * i, pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                         pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv),
+                         pack_bf16x2(f[8] * inv, f[9] * inv), pack_bf16x2(f[10] * inv, f[11] * inv),
+                         pack_bf16x2(f[12] * inv, f[13] * inv), pack_bf16x2(f[14] * inv, f[15] * inv));
+          }
+          p.lse[static_cast<size_t>(w.bh) * N + row] = lse_v;
         }
-        p.lse[static_cast<size_t>(w.bh) * N + row] = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       }
       ATTN_TRACE_EV(trw, 8, rr, 4 + 3 * t);
       ++nq;
@@ -580,7 +607,7 @@ cudaError_t launch_tc(const TcParams& p, int num_sms, cudaStream_t stream) {
   auto kern = attn_fwd_tc_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long items = static_cast<long long>(p.BH) * p.n_pairs;
+  const long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
   const long long grid = items < num_sms ? items : num_sms;  // persistent: at most one CTA per SM
   kern<<<dim3(static_cast<unsigned>(grid)), dim3(C::kThreads), C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
