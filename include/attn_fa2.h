@@ -121,6 +121,31 @@ int attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* 
                    int n_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free split-KV forward.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory when
+ * they call us -- a plugin inside a host application that owns all device
+ * memory through its own pool and gives plugins no allocator, or a
+ * latency-critical loop that cannot pay cudaMalloc's implicit synchronisation.
+ * It computes exactly what attn_fwd_split computes, but the scratch for the
+ * per-range partial results is a 64 MiB array the library itself declares in
+ * device memory, so the caller passes only inputs and outputs and the call
+ * allocates nothing.
+ *   - Sizes whose planned workspace (attn_fwd_split_plan) exceeds 64 MiB are
+ *     rejected with ATTN_ERR_UNSUPPORTED; other arguments as attn_fwd_split.
+ *   - Every GPU that loads the library keeps the 64 MiB array until exit.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the array, which keeps the last call's contents; every
+ *     byte a call reads it has written first, so nothing needs clearing.
+ *     Calls whose work overlaps on the GPU (several streams or threads) race on
+ *     the array: serialise them.
+ */
+int attn_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                           int d, float scale, float q_descale, float k_descale, float v_descale, int causal,
+                           int dtype, int n_splits, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait
  * since the last call (its outputs are then undefined), or ATTN_ERR_CUDA if the

@@ -245,6 +245,12 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
 
 }  // namespace
 
+namespace attn {
+// Records `msg` as this thread's last error and returns `status` (for other
+// translation units of the library).
+int set_last_error(int status, const char* msg) { return fail(status, "%s", msg); }
+}  // namespace attn
+
 extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
