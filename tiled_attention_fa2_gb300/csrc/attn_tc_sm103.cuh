@@ -113,12 +113,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   }
 }
 
-// Exponentials of keys [64h, 64h + 64) of this thread's score row, their
-// packed row sums, and P for those keys written to TMEM over the S columns
-// already consumed (bf16: 32 columns at 32h; e4m3: 16 columns at 16h).
+// Exponentials of keys [64h, 64h + 64) of this thread's score row, in place,
+// and their packed row sums.
 template <class C, int kHalf>
-__device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, uint64_t negx2, uint64_t& rs0,
-                                             uint64_t& rs1, uint32_t t_s) {
+__device__ __forceinline__ void exp_half(float (&s)[128], uint64_t sl2x2, uint64_t negx2, uint64_t& rs0,
+                                         uint64_t& rs1) {
 #pragma unroll
   for (int c = 64 * kHalf; c < 64 * kHalf + 64; c += 4) {
     const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2);
@@ -130,6 +129,12 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
     rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
     rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
   }
+}
+
+// P for keys [64h, 64h + 64) written to TMEM over the S columns already
+// consumed (bf16: 32 columns at 32h; e4m3: 16 columns at 16h).
+template <class C, int kHalf>
+__device__ __forceinline__ void store_half(const float (&s)[128], uint32_t t_s) {
   if constexpr (C::kIsFp8) {
     uint32_t pk[16];
 #pragma unroll
@@ -144,6 +149,13 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
     for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 * kHalf + 2 * i], s[64 * kHalf + 2 * i + 1]);
     tmem_st32_sync(t_s + 32 * kHalf, pk);
   }
+}
+
+template <class C, int kHalf>
+__device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, uint64_t negx2, uint64_t& rs0,
+                                             uint64_t& rs1, uint32_t t_s) {
+  exp_half<C, kHalf>(s, sl2x2, negx2, rs0, rs1);
+  store_half<C, kHalf>(s, t_s);
 }
 
 // Optional event trace (compile with -DATTN_TRACE): per-CTA cycle stamps of
@@ -486,7 +498,68 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
           for (int c = 0; c < 128; ++c)
             if (key0 + c > lim_key) s[c] = -INFINITY;
         }
-        // Row max: eight independent three-input max chains, then a short tree.
+        // Fast path (e4m3, every key tile after the first): with the drift bound
+        // of 4 doublings the reference max rarely moves, so the exponentials of
+        // keys 0..63 are computed with the current reference while the same pass
+        // finds the row max; only if some row of the warp grew past the bound is
+        // the tile redone on the exact path below (S is still intact in TMEM: P
+        // has not been written yet).  bf16 keeps a bound of one doubling, which
+        // some row of a warp exceeds too often for the guess to pay.
+        uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
+        bool fast = false;
+        if (C::kIsFp8 && j > 0) {
+          const uint64_t neg_ref = f2_pack(C::kPExp - m2, C::kPExp - m2);
+          float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            ma = fmax3(ma, s[c], s[c + 1]);
+            mb = fmax3(mb, s[c + 2], s[c + 3]);
+            mc = fmax3(mc, s[64 + c], s[64 + c + 1]);
+            md = fmax3(md, s[64 + c + 2], s[64 + c + 3]);
+            const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, neg_ref);
+            const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, neg_ref);
+            s[c] = ex2_approx(f2_lo(a));
+            s[c + 1] = ex2_approx(f2_hi(a));
+            s[c + 2] = ex2_approx(f2_lo(b));
+            s[c + 3] = ex2_approx(f2_hi(b));
+            rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
+            rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
+          }
+          const float mx = fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
+          fast = !__any_sync(0xffffffffu, mx * sl2 > m2 + C::kTau);
+          if (fast) {
+            ATTN_TRACE_EV(trw && nq == 0, t, j, 1);
+            store_half<C, 0>(s, t_s);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_lo(t));
+            ATTN_TRACE_EV(trw && nq == 0, t, j, 2);
+            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 7, j, t * 4 + (warp & 3));
+            softmax_half<C, 1>(s, sl2x2, neg_ref, rs0, rs1, t_s);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_hi(t));
+            ATTN_TRACE_EV(trw && nq == 0, t, j, 3);
+            const uint64_t rs = f2_add(rs0, rs1);
+            l += f2_lo(rs) + f2_hi(rs);
+            continue;
+          }
+          // Slow path: reload the raw scores of keys 0..63 and mask them again.
+          uint32_t u2[64];
+          tmem_ld64_sync(t_s, u2);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(u2[c]);
+          if (diag || ragged) {
+            const int key0 = jj * 128;
+            const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (key0 + c > lim_key) s[c] = -INFINITY;
+          }
+          rs0 = rs1 = 0;
+        }
+        // Exact path: row max first (eight independent three-input max chains,
+        // then a short tree), then the reference and the rescale of O and l.
         float mx8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
@@ -527,7 +600,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
           }
         }
         const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
-        uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
         softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
         tc_fence_before();
         __syncwarp();
