@@ -580,27 +580,28 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = ex2_approx(m2 - m_use);
         ATTN_TRACE_EV(trw && nq == 0, t, j, 1);
+        const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
+        softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O holds the sum up to key tile j-1 at the old reference: rescale it.
-          // S_j being complete implies O += P_{j-1} V_{j-1} is complete (the MMAs
-          // of one thread complete in issue order and S_j was committed later).
-          // 32 columns at a time: the 128 scores of this row are still live.
+          // O holds the sum up to key tile j-1 at the old reference: rescale it
+          // before the first P V half is released.  S_j being complete implies
+          // O += P_{j-1} V_{j-1} is complete (the MMAs of one thread complete in
+          // issue order and S_j was committed later).  Keys 0..63 are consumed by
+          // now, which leaves registers for 64 columns of O at a time.
           const uint64_t ax2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-          for (int c0 = 0; c0 < C::D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32_sync(t_o + c0, o);
+          for (int c0 = 0; c0 < C::D; c0 += 64) {
+            uint32_t o[64];
+            tmem_ld64_sync(t_o + c0, o);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < 64; i += 2) {
               const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2);
               o[i] = static_cast<uint32_t>(v);
               o[i + 1] = static_cast<uint32_t>(v >> 32);
             }
-            tmem_st32_sync(t_o + c0, o);
+            tmem_st64_sync(t_o + c0, o);
           }
         }
-        const uint64_t negx2 = f2_pack(C::kPExp - m_use, C::kPExp - m_use);
-        softmax_half<C, 0>(s, sl2x2, negx2, rs0, rs1, t_s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_lo(t));
