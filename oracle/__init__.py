@@ -18,6 +18,11 @@ Sources the oracle follows (page title, then the section or listing cited):
 * "1.8x Faster Attention on an RTX 5080: an FP8 Flash Attention Kernel in
   CuTe-DSL", sections "The attention itself" (online softmax worked example) and
   "Who am I, what's mine?" (FP8 descales folded into the score scale).
+* The backward pass ("FlashAttention-2 from PyTorch to Triton", item 5 of the
+  list of what its first kernel leaves out; "Kernels and Memory in LLM
+  Inference", "Training detour (brief)"): P rebuilt from L, D = rowsum(dO * O),
+  dK and dV per key tile, dQ accumulated; the gradient formulas are the chain
+  rule on the forward's definition.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
 worked values printed on those pages, closed forms, invariants and a
@@ -32,4 +37,6 @@ from .attention import (  # noqa: F401
     attention_reference,
     attention_rows,
     attention_tiled,
+    attention_backward,
+    attention_backward_tiled,
 )

@@ -236,3 +236,93 @@ def attention_tiled(q, k, v, scale: float, causal: bool = False, bq: int = 16, b
                 o_all[h, rows] = o_i / l_i
                 l_all[h, rows] = (m_i + np.log(l_i))[:, 0]
     return o_all.reshape(lead + (n, dv)), l_all.reshape(lead + (n,))
+
+
+# --------------------------------------------------------------------------
+# Backward pass: gradients of O with respect to Q, K and V.
+# --------------------------------------------------------------------------
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool = False):
+    """dQ, dK, dV of the attention forward for the upstream gradient dO, float64.
+
+    The pages name the ingredients of FlashAttention's backward ("FlashAttention-2
+    from PyTorch to Triton", item 5 of the list of what the first kernel leaves
+    out; "Kernels and Memory in LLM Inference", "Training detour (brief)"): the
+    probabilities are rebuilt from L as P = exp(S - L), a row term
+    D = rowsum(dO * O) is precomputed, dK and dV are built per key tile and dQ
+    is accumulated.  The formulas themselves are the chain rule applied to the
+    forward's definition (S = scale Q K^T with masked scores excluded,
+    P = row softmax of S, O = P V):
+
+        dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO_ic O_ic (= sum_j P_ij dP_ij),
+        dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
+
+    ``q, k, v, do``: [..., N, d].  Returns (dQ, dK, dV) with the input shapes.
+    One head at a time; P is materialised (N x N), so N is kept small.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    lead = q.shape[:-2]
+    n, d = q.shape[-2], q.shape[-1]
+    nk, dv = k.shape[-2], v.shape[-1]
+    if causal and n != nk:
+        raise ValueError("causal attention is defined here for square inputs only")
+    qf, kf, vf, dof = q.reshape(-1, n, d), k.reshape(-1, nk, d), v.reshape(-1, nk, dv), do.reshape(-1, n, dv)
+    dq, dk, dvv = np.empty_like(qf), np.empty_like(kf), np.empty_like(vf)
+    keep = _causal_keep(np.arange(n), nk) if causal else None
+    for h in range(qf.shape[0]):
+        s = _scores(qf[h], kf[h], scale, keep)
+        m = s.max(axis=-1, keepdims=True)
+        e = np.exp(s - m)
+        p = e / e.sum(axis=-1, keepdims=True)
+        o = np.matmul(p, vf[h])
+        dvv[h] = np.matmul(p.T, dof[h])
+        dp = np.matmul(dof[h], vf[h].T)
+        drow = (dof[h] * o).sum(axis=-1, keepdims=True)
+        ds = p * (dp - drow)
+        dq[h] = float(scale) * np.matmul(ds, kf[h])
+        dk[h] = float(scale) * np.matmul(ds.T, qf[h])
+    return dq.reshape(lead + (n, d)), dk.reshape(lead + (nk, d)), dvv.reshape(lead + (nk, dv))
+
+
+def attention_backward_tiled(q, k, v, do, scale: float, causal: bool = False, bq: int = 16, bk: int = 16):
+    """The same gradients in the tiled order the pages describe, float64.
+
+    "FlashAttention-2 from PyTorch to Triton", item 5 of what the first kernel
+    leaves out: with L from the forward and D = rowsum(dO * O) computed first,
+    iterate over the query tiles for each key tile; per (key tile j, query
+    tile i) rebuild P = exp(S - L) ("Kernels and Memory in LLM Inference",
+    "Training detour (brief)": the attention tile is recomputed on chip when it
+    is needed), add P^T dO_i to dV_j and scale dS^T Q_i to dK_j, and accumulate
+    scale dS K_j into dQ_i.  Ragged last tiles are allowed.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    lead = q.shape[:-2]
+    n, d = q.shape[-2], q.shape[-1]
+    nk, dv = k.shape[-2], v.shape[-1]
+    o_all, l_all = attention_reference(q, k, v, scale, causal)
+    qf, kf, vf, dof = q.reshape(-1, n, d), k.reshape(-1, nk, d), v.reshape(-1, nk, dv), do.reshape(-1, n, dv)
+    of, lf = o_all.reshape(-1, n, dv), l_all.reshape(-1, n)
+    dq, dk, dvv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    for h in range(qf.shape[0]):
+        drow = (dof[h] * of[h]).sum(axis=-1)
+        for j0 in range(0, nk, bk):
+            cols = np.arange(j0, min(j0 + bk, nk))
+            for i0 in range(0, n, bq):
+                rows = np.arange(i0, min(i0 + bq, n))
+                s = float(scale) * np.matmul(qf[h, rows], kf[h, cols].T)
+                p = np.exp(s - lf[h, rows][:, None])
+                if causal:
+                    p = np.where(cols[None, :] <= rows[:, None], p, 0.0)
+                dvv[h, cols] += np.matmul(p.T, dof[h, rows])
+                dp = np.matmul(dof[h, rows], vf[h, cols].T)
+                ds = p * (dp - drow[rows][:, None])
+                dk[h, cols] += float(scale) * np.matmul(ds.T, qf[h, rows])
+                dq[h, rows] += float(scale) * np.matmul(ds, kf[h, cols])
+    return dq.reshape(lead + (n, d)), dk.reshape(lead + (nk, d)), dvv.reshape(lead + (nk, dv))
