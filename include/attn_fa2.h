@@ -146,6 +146,27 @@ int attn_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o,
                            int dtype, int n_splits, void* stream);
 
 /*
+ * Attention backward ("FlashAttention-2 from PyTorch to Triton", item 5 of what
+ * its first kernel leaves out; "Kernels and Memory in LLM Inference", "Training
+ * detour (brief)"): the gradients of the forward above with respect to q, k, v
+ * for the upstream gradient dout, rebuilding P = exp(S - L) tile by tile from the
+ * forward's lse.  With S = scale q k^T and P its row softmax:
+ *     dv = P^T dout,  dS = P * (dout v^T - rowsum(dout * o)),
+ *     dq = scale dS k,  dk = scale dS^T q.
+ *   q, k, v, o, dout : device, [B,H,N,d] bf16 (o and lse as attn_fwd returned them).
+ *   lse              : device, [B,H,N] fp32, natural log.
+ *   dq, dk, dv       : device, [B,H,N,d] bf16 outputs, 16-byte aligned.
+ *   workspace        : device, 256-byte aligned, >= attn_bwd_workspace_size()
+ *                      bytes, owned by the caller; scratch (fp32 dq accumulator
+ *                      and one fp32 per row), overwritten by every call.
+ *   d in {64, 128}; B*H <= 65535.  Other arguments and errors as attn_fwd.
+ */
+int attn_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes_out);
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+             float scale, int causal, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait
  * since the last call (its outputs are then undefined), or ATTN_ERR_CUDA if the

@@ -136,3 +136,31 @@ def call_split(lib, **kw):
 ])
 def test_split_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
     assert call_split(lib, **kw) == status
+
+
+def call_bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, wsb=1 << 40,
+             B=1, H=2, N=256, d=128, scale=0.1, causal=0)
+    a.update(kw)
+    return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["ws"],
+                        a["wsb"], a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(dout=None), 1), (dict(dv=None), 1), (dict(ws=None), 1), (dict(N=0), 1),
+    (dict(causal=3), 1), (dict(scale=0.0), 1), (dict(wsb=1024), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(dq=FAKE + 8), 3), (dict(dout=FAKE + 4), 3), (dict(ws=FAKE + 16), 3), (dict(B=300, H=300, N=8), 2),
+])
+def test_backward_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert call_bwd(lib, **kw) == status
+    assert lib.attn_last_error() != b""
+
+
+def test_backward_workspace_size(lib):
+    # fp32 dQ accumulator (rows x d) then one fp32 per row, each rounded up to 256 bytes.
+    for B, H, N, d in [(1, 1, 1, 64), (2, 3, 300, 128), (4, 16, 2048, 128)]:
+        rows = B * H * N
+        want = -(-rows * d * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+        assert binding.bwd_workspace_size(B, H, N, d) == want
+    with pytest.raises(binding.AttnError):
+        binding.bwd_workspace_size(1, 1, 16, 96)

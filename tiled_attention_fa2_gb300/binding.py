@@ -34,6 +34,8 @@ SIGNATURES = {
     "attn_fwd_split": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _I, _VP, ctypes.c_size_t,
                             _VP]),
     "attn_fwd_split_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _I, _VP]),
+    "attn_bwd_workspace_size": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    "attn_bwd": (_I, [_VP] * 10 + [ctypes.c_size_t, _I, _I, _I, _I, _F, _I, _VP]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_error": (ctypes.c_char_p, []),
 }
@@ -187,6 +189,41 @@ def attn_fwd_split(q, k, v, n_splits=0, descales=None, o=None, lse=None, scale=N
                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                               _stream_handle(stream, q.device)))
     return o, lse
+
+
+def bwd_workspace_size(B, H, N, d) -> int:
+    """Bytes of device workspace attn_bwd needs for these sizes."""
+    nb = ctypes.c_size_t(0)
+    _check(load_library().attn_bwd_workspace_size(int(B), int(H), int(N), int(d), ctypes.byref(nb)))
+    return nb.value
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale=None, causal=False, workspace=None,
+             stream=None):
+    """Backward of the bf16 forward: (dq, dk, dv) for the upstream gradient dout.
+    `o` and `lse` are the forward's outputs.  Allocates outputs and workspace
+    with torch unless given."""
+    B, H, N, d = _shape(q, k, v)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("attn_bwd takes bfloat16 q, k, v")
+    for name, t in (("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != (B, H, N, d) or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor of shape {(B, H, N, d)}")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(B, H, N)}")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    lib = load_library()
+    _check(lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), B, H, N, d, scale, int(bool(causal)),
+                        _stream_handle(stream, q.device)))
+    return dq, dk, dv
 
 
 def get_device_status(stream=None) -> int:

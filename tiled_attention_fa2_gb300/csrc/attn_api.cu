@@ -382,6 +382,60 @@ int attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* 
   return ATTN_OK;
 }
 
+int attn_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes_out) {
+  g_last_error[0] = '\0';
+  if (!bytes_out) return fail(ATTN_ERR_INVALID_ARG, "bytes_out is null");
+  if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d H=%d N=%d)", B, H, N);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the backward supports d = 64 or 128 (got %d)", d);
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  // dQ accumulator (fp32, rows x d) followed by D (fp32, one per row), each 256-byte aligned.
+  const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
+  *bytes_out = acc + (rows * sizeof(float) + 255) / 256 * 256;
+  return ATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+             float scale, int causal, void* stream) {
+  g_last_error[0] = '\0';
+  int st = check_common(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (!dout || !dq || !dk || !dv || !workspace) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+  size_t need = 0;
+  if ((st = attn_bwd_workspace_size(B, H, N, d, &need)) != ATTN_OK) return st;
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(ATTN_ERR_MISALIGNED, "dout, dq, dk and dv must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(ATTN_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B*H must be <= 65535 for the backward grid (got %lld)", BH);
+  attn::BwdParams p;
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((st = make_map(&p.tm_q, q, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_k, k, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_do, dout, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
+  if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
+  const size_t rows = static_cast<size_t>(BH) * N;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.drow = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * d * sizeof(float) + 255) / 256 * 256);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.BH = static_cast<int>(BH);
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.timeout_ns = g_wait_limit_ns;
+  cudaError_t e = attn::launch_bwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ATTN_OK;
+}
+
 uint64_t attn_set_wait_limit_ns(uint64_t ns) {
   const uint64_t old = g_wait_limit_ns;
   g_wait_limit_ns = ns < 1000000ull ? 1000000ull : ns;

@@ -58,11 +58,35 @@ struct SimtParams {
   float scale_log2;     // softmax scale * log2(e)
 };
 
+// Arguments of the backward kernels (bf16, d = 64 or 128).
+struct BwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const void* o;        // bf16 [BH, N, d] (forward output)
+  const void* dout;     // bf16 [BH, N, d] (upstream gradient dO)
+  const float* lse;     // fp32 [BH, N], natural log (forward's L)
+  float* drow;          // fp32 [BH, N] workspace: D = rowsum(dO * O)
+  float* dq_acc;        // fp32 [BH, N, d] workspace: dQ accumulator
+  void* dq;             // bf16 [BH, N, d]
+  void* dk;             // bf16 [BH, N, d]
+  void* dv;             // bf16 [BH, N, d]
+  int* status;          // device status word (timeouts)
+  int BH;
+  int N;
+  float scale;          // softmax scale
+  float scale_log2;     // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
 // Launchers (defined next to their kernels).  Return the launch error.
 // The tensor-core kernels are persistent: min(#work items, num_sms) CTAs.
 cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_simt_f32(const SimtParams& p, int d, bool causal, cudaStream_t stream);
 cudaError_t launch_split_combine(const CombineParams& p, int d, cudaStream_t stream);
+// Backward: D and the zeroed dQ accumulator, the tensor-core pass, dQ to bf16.
+cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stream);
 
 }  // namespace attn

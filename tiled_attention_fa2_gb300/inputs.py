@@ -31,6 +31,13 @@ def make_qkv_f32(B: int, H: int, N: int, d: int, seed: int = 0, q_mult: float = 
     return q, k, v
 
 
+def make_dout_f32(B: int, H: int, N: int, d: int, seed: int = 0):
+    """Float32 upstream gradient dO for the backward, i.i.d. N(0, 1) from
+    ``torch.Generator('cpu').manual_seed(seed)`` (same recipe as Q, K, V)."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    return torch.randn((B, H, N, d), dtype=torch.float32, generator=g)
+
+
 def to_bf16(x: torch.Tensor) -> torch.Tensor:
     """Round-to-nearest-even cast to bfloat16 (torch's cast)."""
     return x.to(torch.bfloat16)
