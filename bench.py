@@ -402,6 +402,129 @@ def make_host_inputs(w):
     return (q, k, v), (1.0, 1.0, 1.0)
 
 
+def run_gpu_bwd(args, w):
+    """The backward pass (bf16 workloads): dQ, dK, dV for a seeded dO, with O and
+    L from one forward call made before the timed region.  A step = the three
+    backward launches (D and the dQ accumulator, the tensor-core pass, dQ to
+    bf16); algorithmic FLOPs = 2.5 x the forward's (five products instead of
+    two), halved for causal like the forward's."""
+    from tiled_attention_fa2_gb300 import binding
+
+    if w["dtype"] != "bf16":
+        raise SystemExit("--pass bwd runs the bf16 workloads only")
+    rank = int(os.environ.get("RANK", "0"))
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    lib = binding.load_library()
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    host, (q, k, v), _ = make_device_inputs(w, device, seed=rank)
+    h_do = inputs.to_bf16(inputs.make_dout_f32(B, H, N, d, seed=rank + 1))
+    dout = h_do.to(device)
+    o, lse = binding.attn_fwd(q, k, v, causal=causal)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    nbytes = binding.bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def launch():
+        st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), nbytes, B, H, N, d, scale,
+                          int(causal), sh)
+        if st != 0:
+            raise RuntimeError(lib.attn_last_error().decode())
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        launch()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    time.sleep(0.2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        launch()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    if binding.get_device_status() != 0:
+        raise RuntimeError("device status set after the timed region")
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = sum(times_ms) / args.steps
+    flops = 2.5 * inputs.attention_flops(B, H, N, d, causal)
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+
+    # end to end: the step's inputs from pinned host memory, the gradients back to it
+    h_in = [t.pin_memory() for t in (*host, o.cpu(), lse.cpu(), h_do)]
+    d_in = [q, k, v, o, lse, dout]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    e2e_steps = max(1, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip(d_in, h_in):
+            dst.copy_(src, non_blocking=True)
+        launch()
+        for dst, src in zip(h_out, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    peaks, peaks_src = load_peaks()
+    peak, peak_note = dtype_peak("bf16", peaks)
+    line = {
+        "metric": "attention bwd TFLOPS (2.5 x forward FLOPs) & % of GB300 dense bf16 tensor peak",
+        "pass": "bwd",
+        "value": round(achieved, 3),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 5),
+        "ms_per_step_median": round(statistics.median(times_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: i.i.d. N(0,1) Q/K/V/dO from seeded CPU generators",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": bool(causal),
+                   "flops_per_step": flops, "l2": "flushed before every timed step (512 MiB device write)",
+                   "parallelism": "single GPU"},
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peaks_src}: {peak_note}",
+                     "note": "whole step (three launches) against the tensor peak", "traffic": None},
+        "clocks": clocks,
+        "e2e": {"value": round(flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out)},
+        "gpu_launches": 3 * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+
+        # one head of the same shape, gradients in float64, scaled to the whole job
+        hq, hk, hv, hd = (t[0, 0].double().numpy() for t in (*host, h_do))
+        t0 = time.perf_counter()
+        oracle.attention_backward(hq, hk, hv, hd, scale, causal)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(flops / (B * H) / dt / 1e12, 6), "unit": UNIT,
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"one head ({N}x{d}) of the workload, oracle.attention_backward, "
+                                          f"{dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,12 +534,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the backward pass instead (auxiliary line, bf16 workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference_arm(args, w)
+    elif args.pass_ == "bwd":
+        run_gpu_bwd(args, w)
     else:
         run_gpu_arm(args, w)
 

@@ -67,6 +67,38 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
   return tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
+// Two 32-lane x 64-column TMEM loads with a single wait (both in one statement,
+// so no use of the registers can move above the wait).
+__device__ __forceinline__ void tmem_ld64x2_sync(uint32_t ta, uint32_t (&a)[64], uint32_t tb, uint32_t (&b)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,"
+      "%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,"
+      "%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, "
+      "[%129];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]),
+        "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]),
+        "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]),
+        "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(a[32]),
+        "=r"(a[33]), "=r"(a[34]), "=r"(a[35]), "=r"(a[36]), "=r"(a[37]), "=r"(a[38]), "=r"(a[39]), "=r"(a[40]),
+        "=r"(a[41]), "=r"(a[42]), "=r"(a[43]), "=r"(a[44]), "=r"(a[45]), "=r"(a[46]), "=r"(a[47]), "=r"(a[48]),
+        "=r"(a[49]), "=r"(a[50]), "=r"(a[51]), "=r"(a[52]), "=r"(a[53]), "=r"(a[54]), "=r"(a[55]), "=r"(a[56]),
+        "=r"(a[57]), "=r"(a[58]), "=r"(a[59]), "=r"(a[60]), "=r"(a[61]), "=r"(a[62]), "=r"(a[63]), "=r"(b[0]),
+        "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
+        "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]),
+        "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]),
+        "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31]), "=r"(b[32]), "=r"(b[33]),
+        "=r"(b[34]), "=r"(b[35]), "=r"(b[36]), "=r"(b[37]), "=r"(b[38]), "=r"(b[39]), "=r"(b[40]), "=r"(b[41]),
+        "=r"(b[42]), "=r"(b[43]), "=r"(b[44]), "=r"(b[45]), "=r"(b[46]), "=r"(b[47]), "=r"(b[48]), "=r"(b[49]),
+        "=r"(b[50]), "=r"(b[51]), "=r"(b[52]), "=r"(b[53]), "=r"(b[54]), "=r"(b[55]), "=r"(b[56]), "=r"(b[57]),
+        "=r"(b[58]), "=r"(b[59]), "=r"(b[60]), "=r"(b[61]), "=r"(b[62]), "=r"(b[63])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
 // S (or dP) = A B^T for 128 x 128 tiles with d-long rows: both operands K-major.
 template <int D>
 __device__ __forceinline__ void mma_rows(uint32_t tmem_d, uint32_t a, uint32_t b) {
@@ -183,15 +215,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
 
   const float sl2 = p.scale_log2;
   const int key_r = j * 128 + tid;  // this thread's key row (dK, dV)
-  int it = 0;
-  for (int i = kCausal ? j : 0; ok && i < n_kt; ++i, ++it) {
-    if (warp == 0) {
-      mbar_arrive_expect_tx_elect(qd_bar, 2 * C::kTileBytes);
-      for (int b = 0; b < C::kBlocks; ++b) {
-        tma_load_3d_elect(sQ + b * 16384, &p.tm_q, qd_bar, b * 64, i * 128, bh);
-        tma_load_3d_elect(sDO + b * 16384, &p.tm_do, qd_bar, b * 64, i * 128, bh);
-      }
+  const int i0 = kCausal ? j : 0;   // first query tile that sees key tile j
+  // Q_i and dO_i of query tile i into shared memory (issued by warp 0).
+  auto load_qdo = [&](int i) {
+    mbar_arrive_expect_tx_elect(qd_bar, 2 * C::kTileBytes);
+    for (int b = 0; b < C::kBlocks; ++b) {
+      tma_load_3d_elect(sQ + b * 16384, &p.tm_q, qd_bar, b * 64, i * 128, bh);
+      tma_load_3d_elect(sDO + b * 16384, &p.tm_do, qd_bar, b * 64, i * 128, bh);
     }
+  };
+  if (warp == 0) load_qdo(i0);
+  int it = 0;
+  for (int i = i0; ok && i < n_kt; ++i, ++it) {
     const int row = i * 128 + tid;  // this thread's query row
     // Rows past N: L = +inf makes every P of the row 0.
     const float l2 = row < N ? p.lse[static_cast<size_t>(bh) * N + row] * 1.4426950408889634f : INFINITY;
@@ -207,32 +242,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     ok = __syncthreads_and(mbar_wait(mma1_bar, it & 1, p.status, lim));
     if (!ok) break;
     tc_fence_after();
-    // P and dS of this thread's query row, 32 keys at a time.
+    // P and dS of this thread's query row, 64 keys at a time (S and dP columns
+    // loaded together, one wait).
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      uint32_t s[32], dp[32];
-      tmem_ld32_sync(tmem + lane_base + C::kColS + c0, s);
-      tmem_ld32_sync(tmem + lane_base + C::kColDP + c0, dp);
-      uint32_t pw[16], dw[16];
+    for (int c0 = 0; c0 < 128; c0 += 64) {
+      uint32_t s[64], dp[64];
+      tmem_ld64x2_sync(tmem + lane_base + C::kColS + c0, s, tmem + lane_base + C::kColDP + c0, dp);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float pv[2], dv[2];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[16], dw[16];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int key = j * 128 + c0 + e + u;
-          const bool keep = key < N && (!kCausal || key <= row);
-          const float pe = keep ? ex2_approx(fmaf(__uint_as_float(s[e + u]), sl2, -l2)) : 0.f;
-          pv[u] = pe;
-          dv[u] = pe * (__uint_as_float(dp[e + u]) - drow);
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 32 * h + e + u;
+            const int key = j * 128 + c0 + c;
+            const bool keep = key < N && (!kCausal || key <= row);
+            const float pe = keep ? ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2)) : 0.f;
+            pv[u] = pe;
+            dv[u] = pe * (__uint_as_float(dp[c]) - drow);
+          }
+          pw[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          dw[e / 2] = pack_bf16x2(dv[0], dv[1]);
         }
-        pw[e / 2] = pack_bf16x2(pv[0], pv[1]);
-        dw[e / 2] = pack_bf16x2(dv[0], dv[1]);
-      }
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c = (c0 >> 3) + q4;  // 8-column chunk index 0..15
-        st_shared_v4(sw128_chunk(sP, tid, c), pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-        st_shared_v4(sw128_chunk(sDS, tid, c), dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int c = ((c0 + 32 * h) >> 3) + q4;  // 8-column chunk index 0..15
+          st_shared_v4(sw128_chunk(sP, tid, c), pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
+          st_shared_v4(sw128_chunk(sDS, tid, c), dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+        }
       }
     }
     // The tensor core reads P and dS through the async proxy; S's columns are
@@ -249,6 +288,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     }
     ok = __syncthreads_and(mbar_wait(mma2_bar, it & 1, p.status, lim));
     if (!ok) break;
+    // Q_i and dO_i are read: the next query tile's copies overlap the dQ adds below.
+    if (warp == 0 && i + 1 < n_kt) load_qdo(i + 1);
     tc_fence_after();
     {
       // tcgen05.ld is warp-collective: every lane loads, only rows < N are added.
