@@ -416,6 +416,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if ((st = make_map(&p.tm_k, k, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
   if ((st = make_map(&p.tm_v, v, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
   if ((st = make_map(&p.tm_do, dout, dt, 2, static_cast<int>(BH), N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_dqacc, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<int>(BH), N, d)) !=
+      ATTN_OK)
+    return st;
   if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
   const size_t rows = static_cast<size_t>(BH) * N;
   p.o = o;

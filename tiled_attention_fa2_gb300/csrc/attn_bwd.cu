@@ -6,8 +6,8 @@
 // Memory in LLM Inference", "Training detour (brief)"): a first pass computes
 // D = rowsum(dO * O); then, per key tile, the query tiles that see it are
 // visited one after the other, P = exp(S - L) is rebuilt on chip, dK and dV
-// accumulate in TMEM, and dQ is accumulated in fp32 global memory with atomic
-// adds; a last pass converts dQ to bf16.  With S = scale Q K^T and P its row
+// accumulate in TMEM, and dQ is accumulated in fp32 global memory by TMA
+// reduce-adds; a last pass converts dQ to bf16.  With S = scale Q K^T and P its row
 // softmax:  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,
 // dK = scale dS^T Q.
 //
@@ -18,8 +18,8 @@
 //   threads: P = 2^(S * scale * log2 e - L * log2 e) (masked keys 0),
 //   dS = P * (dP - D), both to shared memory as bf16 in the 128-byte swizzled
 //   layout -> MMA dV += P^T dO_i, dK += dS^T Q_i (P^T and dS^T are the same bytes
-//   read as MN-major A operands), dQ_i' = dS K_j -> threads: dQ += scale dQ_i'
-//   (vector atomic adds).
+//   read as MN-major A operands), dQ_i' = dS K_j -> threads stage scale dQ_i'
+//   in shared memory -> TMA reduce-add into the fp32 dQ accumulator.
 // After the last query tile: dK * scale and dV to bf16.
 #include <cuda_bf16.h>
 
@@ -47,10 +47,18 @@ struct BwdCfg {
   static constexpr uint32_t kIdescDQ = make_idesc(1, 128, D, 0, 1);    // dS K: A K-major, B MN-major
 };
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+// Bulk tensor reduce-add shared -> global (element type and box from the map),
+// tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The source shared memory of every committed group has been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed group has completed (its global writes are done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -239,6 +247,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       mma_rows<D>(tmem + C::kColDP, sDO, sV);
       mma_commit_elect(mma1_bar);
     }
+    // The previous tile's dQ reduce has read its staging copy (P and dS buffers).
+    if (tid == 0) bulk_wait_read_all();
     ok = __syncthreads_and(mbar_wait(mma1_bar, it & 1, p.status, lim));
     if (!ok) break;
     tc_fence_after();
@@ -291,24 +301,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     // Q_i and dO_i are read: the next query tile's copies overlap the dQ adds below.
     if (warp == 0 && i + 1 < n_kt) load_qdo(i + 1);
     tc_fence_after();
-    {
-      // tcgen05.ld is warp-collective: every lane loads, only rows < N are added.
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + (row < N ? row : 0)) * D;
+    // dQ contribution scale * dS K_j: staged as fp32 in the P and dS buffers (no
+    // MMA reads them any more) in the 128-byte-swizzled layout of a 128-row x
+    // 32-float TMA box, then added to the fp32 accumulator by TMA reduce-adds,
+    // which clip the rows past N.  tcgen05.ld is warp-collective: every lane loads.
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t g[32];
-        tmem_ld32_sync(tmem + lane_base + C::kColS + c0, g);
-        if (row < N) {
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t g[32];
+      tmem_ld32_sync(tmem + lane_base + C::kColS + c0, g);
+      const uint32_t blk = sP + (c0 / 32) * 16384 + tid * 128;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + c0 + e, __uint_as_float(g[e]) * p.scale, __uint_as_float(g[e + 1]) * p.scale,
-                       __uint_as_float(g[e + 2]) * p.scale, __uint_as_float(g[e + 3]) * p.scale);
-        }
-      }
+      for (int q4 = 0; q4 < 8; ++q4)
+        st_shared_v4(blk + ((q4 ^ (tid & 7)) << 4), __float_as_uint(__uint_as_float(g[4 * q4]) * p.scale),
+                     __float_as_uint(__uint_as_float(g[4 * q4 + 1]) * p.scale),
+                     __float_as_uint(__uint_as_float(g[4 * q4 + 2]) * p.scale),
+                     __float_as_uint(__uint_as_float(g[4 * q4 + 3]) * p.scale));
     }
+    fence_proxy_async_smem();
     // Next query tile: Q/dO and S/dP columns are reused.
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+      for (int b = 0; b < D / 32; ++b) tma_reduce_add_3d(&p.tm_dqacc, sP + b * 16384, b * 32, i * 128, bh);
+      bulk_commit_group();
+    }
   }
 
   if (ok) {
@@ -340,7 +356,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     }
   }
 
-  // ---- teardown: every MMA of this CTA has completed before TMEM is freed
+  // ---- teardown: the dQ reduce-adds have completed, every MMA of this CTA has
+  // completed before TMEM is freed
+  if (tid == 0) bulk_wait_all();
   if (warp == 0) {
     mma_commit_elect(done_bar);
     mbar_wait(done_bar, 0, p.status, lim);

@@ -64,6 +64,7 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  CUtensorMap tm_dqacc; // fp32 [BH, N, d] dQ accumulator (TMA reduce-add target)
   const void* o;        // bf16 [BH, N, d] (forward output)
   const void* dout;     // bf16 [BH, N, d] (upstream gradient dO)
   const float* lse;     // fp32 [BH, N], natural log (forward's L)
