@@ -47,10 +47,16 @@ PUBLISHED_TFLOPS = {"dit_e4m3": 26.27e12 / 123.6e-3 / 1e12}  # RTX 5080, final F
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def kernel_source_hash() -> str:
+# The sources the tensor-core forward kernel and its launch are built from; a
+# change anywhere else (backward, fp32 path, split-KV merge) leaves it as it was.
+FWD_SOURCES = ("attn_api.cu", "attn_kernels.h", "attn_tc_bf16.cu", "attn_tc_e4m3.cu", "attn_tc_sm103.cuh",
+               "ptx_sm103.cuh")
+
+
+def kernel_source_hash(files=FWD_SOURCES) -> str:
     d = os.path.join(ROOT, "tiled_attention_fa2_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -518,7 +524,8 @@ def run_gpu_bwd(args, w):
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out)},
         "gpu_launches": 3 * args.steps,
         "wall_s_timed_region": round(wall, 4),
-        "kernel_source_hash": kernel_source_hash(),
+        "kernel_source_hash": kernel_source_hash(tuple(sorted(os.listdir(os.path.join(
+            ROOT, "tiled_attention_fa2_gb300", "csrc"))))),
     }
     if not args.no_cpu_baseline:
         import oracle
