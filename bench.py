@@ -351,6 +351,25 @@ def oracle_sample(w, host, descales, heads, rows_per_head):
     return time.perf_counter() - t0, flops
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name on x86, implementer and
+    part numbers on Arm)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for ln in info:
+        if ":" in ln:
+            k, v = (x.strip() for x in ln.split(":", 1))
+            fields.setdefault(k, v)
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"Arm implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return "unknown"
+
+
 def cpu_baseline(w, host, descales, budget_s=15.0):
     """Time the oracle as it stands on this host's cores, on a bounded sample of
     about `budget_s` seconds: the whole workload (repeated to fill the budget)
@@ -372,9 +391,13 @@ def cpu_baseline(w, host, descales, budget_s=15.0):
             heads = list(range(max(1, min(BH, int(budget_s / max(secs, 1e-3))))))
             secs, flops = oracle_sample(w, host, descales, heads, rows)
         sample = f"{len(heads)} of {BH} heads x {rows} sampled query rows"
-    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{sample} (causal rows see keys <= row); {secs:.1f} s; numpy float64, BLAS threads = all cores",
-            "seconds": round(secs, 2)}
+    out = {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(),
+           "kind": "oracle",
+           "sample": f"{sample} (causal rows see keys <= row); {secs:.1f} s; numpy float64, BLAS threads = all cores",
+           "seconds": round(secs, 2)}
+    total = inputs.attention_flops(w["B"], w["H"], N, w["d"], w["causal"])
+    out["extrapolated_full_call_s"] = round(total / (flops / secs), 3)  # one whole call at the sample's rate
+    return out
 
 
 def run_reference_arm(args, w):
@@ -401,8 +424,8 @@ def run_reference_arm(args, w):
             "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
                        "causal": bool(w["causal"])},
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
