@@ -50,3 +50,25 @@ def test_backward_is_deterministic_except_for_dq_rounding():
     b, _ = run_case(1, 2, 300, 128, True, seed=5)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     assert np.abs(a[0] - b[0]).max() <= 1e-3 * max(1.0, np.abs(a[0]).max())
+
+
+def test_backward_on_the_causal_prefill_shape_sampled_heads():
+    # The full causal prefill shape (B=4, H=16, N=2048, d=128) through the CUDA
+    # forward and backward; three heads (first, a middle one, last) compared in full.
+    B, H, N, d = 4, 16, 2048, 128
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=11)
+    do = inputs.make_dout_f32(B, H, N, d, seed=12)
+    qb, kb, vb, dob = (inputs.to_bf16(t) for t in (q, k, v, do))
+    dev = [t.cuda() for t in (qb, kb, vb, dob)]
+    o, lse = binding.attn_fwd(dev[0], dev[1], dev[2], causal=True)
+    grads = binding.attn_bwd(dev[0], dev[1], dev[2], o, lse, dev[3], causal=True)
+    torch.cuda.synchronize()
+    assert binding.get_device_status() == 0
+    got = [g.float().cpu().reshape(B * H, N, d) for g in grads]
+    flat = [t.reshape(B * H, N, d) for t in (qb, kb, vb, dob)]
+    for h in (0, 27, B * H - 1):
+        ref = oracle.attention_backward(*(t[h].double().numpy() for t in flat), 1.0 / np.sqrt(d), True)
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            err = np.abs(g[h].double().numpy() - r).max()
+            tol = 2e-2 * np.abs(r).max() + 2e-3
+            assert err <= tol, f"head {h} {name}: {err:.3e} > {tol:.3e}"
