@@ -33,10 +33,11 @@ class Case:
     stored: tuple               # CPU tensors handed to the GPU (q, k, v)
     codes: tuple                # numpy arrays handed to the oracle ([BH, N, d] each)
     descales: tuple = (1.0, 1.0, 1.0)
+    scale_override: float | None = None  # softmax scale other than 1/sqrt(d)
 
     @property
     def scale(self):
-        return 1.0 / math.sqrt(self.d)
+        return self.scale_override if self.scale_override is not None else 1.0 / math.sqrt(self.d)
 
 
 def make_case(B, H, N, d, dtype, seed=0, q_mult=1.0) -> Case:

@@ -72,3 +72,22 @@ def test_backward_on_the_causal_prefill_shape_sampled_heads():
             err = np.abs(g[h].double().numpy() - r).max()
             tol = 2e-2 * np.abs(r).max() + 2e-3
             assert err <= tol, f"head {h} {name}: {err:.3e} > {tol:.3e}"
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.5])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_non_default_scale(scale, causal):
+    B, H, N, d = 1, 2, 300, 128
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=21)
+    do = inputs.make_dout_f32(B, H, N, d, seed=22)
+    qb, kb, vb, dob = (inputs.to_bf16(t) for t in (q, k, v, do))
+    dev = [t.cuda() for t in (qb, kb, vb, dob)]
+    o, lse = binding.attn_fwd(dev[0], dev[1], dev[2], scale=scale, causal=causal)
+    grads = binding.attn_bwd(dev[0], dev[1], dev[2], o, lse, dev[3], scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert binding.get_device_status() == 0
+    ref = oracle.attention_backward(*(t.double().numpy() for t in (qb, kb, vb, dob)), scale, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        err = np.abs(g.float().cpu().double().numpy() - r).max()
+        tol = 2e-2 * np.abs(r).max() + 2e-3
+        assert err <= tol, f"{name}: {err:.3e} > {tol:.3e}"
