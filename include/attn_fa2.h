@@ -158,7 +158,8 @@ int attn_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o,
  *   dq, dk, dv       : device, [B,H,N,d] bf16 outputs, 16-byte aligned.
  *   workspace        : device, 256-byte aligned, >= attn_bwd_workspace_size()
  *                      bytes, owned by the caller; scratch (fp32 dq accumulator
- *                      and one fp32 per row), overwritten by every call.
+ *                      and two fp32 per row, each head's rows padded to a
+ *                      multiple of 128), overwritten by every call.
  *   d in {64, 128}; B*H <= 65535.  Other arguments and errors as attn_fwd.
  */
 int attn_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes_out);

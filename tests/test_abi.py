@@ -157,10 +157,12 @@ def test_backward_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
 
 
 def test_backward_workspace_size(lib):
-    # fp32 dQ accumulator (rows x d) then one fp32 per row, each rounded up to 256 bytes.
+    # fp32 dQ accumulator (rows x d), then two fp32 vectors with one entry per row of
+    # each head padded to a multiple of 128 rows, each rounded up to 256 bytes.
     for B, H, N, d in [(1, 1, 1, 64), (2, 3, 300, 128), (4, 16, 2048, 128)]:
         rows = B * H * N
-        want = -(-rows * d * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+        prows = B * H * (-(-N // 128) * 128)
+        want = -(-rows * d * 4 // 256) * 256 + 2 * (-(-prows * 4 // 256) * 256)
         assert binding.bwd_workspace_size(B, H, N, d) == want
     with pytest.raises(binding.AttnError):
         binding.bwd_workspace_size(1, 1, 16, 96)

@@ -388,9 +388,11 @@ int attn_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes_out) {
   if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d H=%d N=%d)", B, H, N);
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the backward supports d = 64 or 128 (got %d)", d);
   const size_t rows = static_cast<size_t>(B) * H * N;
-  // dQ accumulator (fp32, rows x d) followed by D (fp32, one per row), each 256-byte aligned.
+  const size_t prows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
+  // dQ accumulator (fp32, rows x d), then L log2 e and D (fp32, one per row with
+  // each head padded to whole 128-row tiles), each 256-byte aligned.
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
-  *bytes_out = acc + (rows * sizeof(float) + 255) / 256 * 256;
+  *bytes_out = acc + 2 * ((prows * sizeof(float) + 255) / 256 * 256);
   return ATTN_OK;
 }
 
@@ -421,11 +423,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     return st;
   if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
   const size_t rows = static_cast<size_t>(BH) * N;
+  const size_t prows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128 * 128);
+  const size_t acc_bytes = (rows * d * sizeof(float) + 255) / 256 * 256;
+  const size_t vec_bytes = (prows * sizeof(float) + 255) / 256 * 256;
   p.o = o;
   p.dout = dout;
   p.lse = lse;
   p.dq_acc = static_cast<float*>(workspace);
-  p.drow = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * d * sizeof(float) + 255) / 256 * 256);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+  p.drow = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes + vec_bytes);
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

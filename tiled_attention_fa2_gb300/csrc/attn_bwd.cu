@@ -11,16 +11,30 @@
 // softmax:  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,
 // dK = scale dS^T Q.
 //
-// Main kernel, one CTA of 128 threads per (key tile j, b*h): thread r owns key
-// row r of dK and dV (TMEM lane r) and query row r of each visited query tile.
-// Per query tile i:
-//   TMA Q_i, dO_i -> MMA S = Q_i K_j^T and dP = dO_i V_j^T (TMEM) ->
-//   threads: P = 2^(S * scale * log2 e - L * log2 e) (masked keys 0),
-//   dS = P * (dP - D), both to shared memory as bf16 in the 128-byte swizzled
-//   layout -> MMA dV += P^T dO_i, dK += dS^T Q_i (P^T and dS^T are the same bytes
-//   read as MN-major A operands), dQ_i' = dS K_j -> threads stage scale dQ_i'
-//   in shared memory -> TMA reduce-add into the fp32 dQ accumulator.
-// After the last query tile: dK * scale and dV to bf16.
+// Main kernel, one CTA per (key tile j, b*h), scores held transposed: TMEM lane
+// r is key r of the tile, so S^T = K_j Q_i^T and dP^T = V_j dO_i^T put one key
+// row of each per thread, and the P^T and dS^T that thread computes are already
+// the A operands of dV += P^T dO_i and dK += dS^T Q_i, straight from TMEM.
+// Warp roles (320 threads):
+//   warps 0-7  elementwise pass: warp w owns TMEM lanes 32 (w % 4).. (keys) and
+//              query columns 64 (w / 4)..; P^T = 2^(S^T scale log2 e - L log2 e),
+//              dS^T = P^T (dP^T - D), written back to TMEM as bf16 over dP^T, and
+//              dS^T also to shared memory for dQ; then they move dQ_i out of
+//              TMEM and stage it for the reduce-adds;
+//   warp 8     TMA producer: K_j, V_j once, then Q_i, dO_i and the tile's L and D
+//              vectors into one of two slots, one query tile ahead; it also
+//              issues the dQ reduce-adds from the slots;
+//   warp 9     MMA issuer, per query tile i:
+//                dV += P^T dO_i, dK += dS^T Q_i   (A from TMEM; the last readers of the slot)
+//                dQ_i = dS K_j          (into the S^T columns, drained by warps 0-7)
+//                dP^T_{i+1} = V_j dO_{i+1}^T   (over P^T, dS^T: issued after their readers)
+//                S^T_{i+1} = K_j Q_{i+1}^T    (once the dQ_i drain has read its columns)
+// The pass warps move dQ_i from TMEM into registers, then (the slot's Q and dO
+// being read by then) stage it, scaled, in that slot as fp32 TMA boxes; the
+// producer warp issues the reduce-adds into the fp32 accumulator and waits for
+// them to read the slot before loading the query tile after next into it, so
+// neither the reduce nor its completion sits on the pass warps' path.  After the
+// last query tile: dK * scale and dV to bf16.
 #include <cuda_bf16.h>
 
 #include "attn_kernels.h"
@@ -29,23 +43,39 @@
 namespace attn {
 namespace {
 
-constexpr int kBwdThreads = 128;
-constexpr int kPSBytes = 128 * 128 * 2;  // one [128 query][128 key] bf16 tile (P or dS)
+constexpr int kBwdThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kPSBytes = 128 * 128 * 2;  // one [128 key][128 query] bf16 tile (dS^T)
+constexpr int kMaxSmem = 232448;         // opt-in dynamic shared memory per CTA
 
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
   static constexpr int kBlocks = D / 64;          // 128-byte column blocks per row
-  static constexpr int kK = 0, kV = kTileBytes, kQ = 2 * kTileBytes, kDO = 3 * kTileBytes;
-  static constexpr int kP = 4 * kTileBytes, kDS = kP + kPSBytes;
-  static constexpr int kBar = kDS + kPSBytes;
-  static constexpr int kSmemBytes = kBar + 1024 /*barriers*/ + 1024 /*alignment slack*/;
-  // TMEM columns: dV | dK | S (then dS K) | dP
+  // Shared memory (from a 1024-byte aligned base): K | V | slot 0 (Q, dO) | slot 1 (Q, dO)
+  // | dS^T | L2 slot 0, 1 | D slot 0, 1 | barriers.  A slot, once its Q and dO are
+  // read, stages that query tile's fp32 dQ (128 x d x 4 bytes = the slot's size)
+  // as d/32 TMA boxes of 128 rows x 32 floats.
+  static constexpr int kK = 0, kV = kTileBytes, kSlot = 2 * kTileBytes, kSlotBytes = 2 * kTileBytes;
+  static constexpr int kDS = 6 * kTileBytes;
+  static constexpr int kBoxes = D / 32;  // dQ staging boxes per query tile
+  static constexpr int kL2 = kDS + kPSBytes, kDrow = kL2 + 2 * 512;
+  static constexpr int kBar = kDrow + 2 * 512;
+  static constexpr int kUsed = kBar + 16 * 8 + 16;
+  static constexpr int kSmemBytes = (kUsed + 1024 < kMaxSmem) ? kUsed + 1024 : kMaxSmem;
+  static_assert(kUsed <= kMaxSmem, "shared memory layout too large");
+  // TMEM columns: dV | dK | S^T (then dQ) | dP^T (then P^T and dS^T, bf16)
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
-  static constexpr uint32_t kIdescQK = make_idesc(1, 128, 128, 0, 0);  // S, dP: both operands K-major
-  static constexpr uint32_t kIdescT = make_idesc(1, 128, D, 1, 1);     // dV, dK: A = P^T / dS^T, B = dO / Q
-  static constexpr uint32_t kIdescDQ = make_idesc(1, 128, D, 0, 1);    // dS K: A K-major, B MN-major
+  static constexpr uint32_t kIdescQK = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+  static constexpr uint32_t kIdescTS = make_idesc(1, 128, D, 0, 1);    // dV, dK: A in TMEM, B = dO / Q MN-major
+  static constexpr uint32_t kIdescDQ = make_idesc(1, 128, D, 1, 1);    // dS K: A = dS^T tile MN-major, B = K MN-major
 };
+
+// TMEM column (relative to the dP^T block) of the bf16 P^T (dS^T: + 16) values
+// of queries [16 kk, 16 kk + 16): pass warpgroup g writes queries [64g, 64g + 64)
+// in two 32-query chunks, each chunk's P^T then dS^T over the 32 dP^T columns it
+// has just read.
+__device__ __forceinline__ uint32_t pds_col(int kk) { return (kk >> 2) * 64 + ((kk >> 1) & 1) * 32 + (kk & 1) * 8; }
 
 // Bulk tensor reduce-add shared -> global (element type and box from the map),
 // tracked by the issuing thread's bulk async-groups.
@@ -60,13 +90,44 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // Every committed group has completed (its global writes are done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Contiguous global -> shared copy (16-byte aligned addresses, size a multiple
+// of 16), completion counted in bytes on `bar`; elected lane.
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+
+// The same threads agree on a flag: true only if it is true in every one of
+// them, so a failed (timed-out) wait makes all pass warps leave together and
+// none is left waiting at a pass barrier.
+__device__ __forceinline__ bool pass_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 2, 256, q;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+
 
 // Byte address of the 16-byte chunk holding columns [8c, 8c + 8) of row r of a
 // [128 x 128] bf16 tile stored as two 128-byte-swizzled column blocks (the
@@ -75,39 +136,29 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
   return tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-// Two 32-lane x 64-column TMEM loads with a single wait (both in one statement,
+// Two 32-lane x 32-column TMEM loads with a single wait (both in one statement,
 // so no use of the registers can move above the wait).
-__device__ __forceinline__ void tmem_ld64x2_sync(uint32_t ta, uint32_t (&a)[64], uint32_t tb, uint32_t (&b)[64]) {
+__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,"
-      "%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,"
-      "%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, "
-      "[%129];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]),
         "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]),
         "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]),
-        "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(a[32]),
-        "=r"(a[33]), "=r"(a[34]), "=r"(a[35]), "=r"(a[36]), "=r"(a[37]), "=r"(a[38]), "=r"(a[39]), "=r"(a[40]),
-        "=r"(a[41]), "=r"(a[42]), "=r"(a[43]), "=r"(a[44]), "=r"(a[45]), "=r"(a[46]), "=r"(a[47]), "=r"(a[48]),
-        "=r"(a[49]), "=r"(a[50]), "=r"(a[51]), "=r"(a[52]), "=r"(a[53]), "=r"(a[54]), "=r"(a[55]), "=r"(a[56]),
-        "=r"(a[57]), "=r"(a[58]), "=r"(a[59]), "=r"(a[60]), "=r"(a[61]), "=r"(a[62]), "=r"(a[63]), "=r"(b[0]),
+        "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]),
         "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
         "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]),
         "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]),
-        "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31]), "=r"(b[32]), "=r"(b[33]),
-        "=r"(b[34]), "=r"(b[35]), "=r"(b[36]), "=r"(b[37]), "=r"(b[38]), "=r"(b[39]), "=r"(b[40]), "=r"(b[41]),
-        "=r"(b[42]), "=r"(b[43]), "=r"(b[44]), "=r"(b[45]), "=r"(b[46]), "=r"(b[47]), "=r"(b[48]), "=r"(b[49]),
-        "=r"(b[50]), "=r"(b[51]), "=r"(b[52]), "=r"(b[53]), "=r"(b[54]), "=r"(b[55]), "=r"(b[56]), "=r"(b[57]),
-        "=r"(b[58]), "=r"(b[59]), "=r"(b[60]), "=r"(b[61]), "=r"(b[62]), "=r"(b[63])
+        "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
       : "r"(ta), "r"(tb)
       : "memory");
 }
 
-// S (or dP) = A B^T for 128 x 128 tiles with d-long rows: both operands K-major.
+// acc = A B^T for 128 x 128 tiles with d-long rows (S^T = K Q^T, dP^T = V dO^T):
+// both operands K-major.
 template <int D>
 __device__ __forceinline__ void mma_rows(uint32_t tmem_d, uint32_t a, uint32_t b) {
 #pragma unroll
@@ -119,36 +170,46 @@ __device__ __forceinline__ void mma_rows(uint32_t tmem_d, uint32_t a, uint32_t b
   }
 }
 
-// acc (+)= X^T Y for X = [128 query][128 key] (P or dS) and Y = [128 query][d]
-// (dO or Q): contraction over the query rows; X read as an MN-major A operand,
-// Y as an MN-major B operand.
+// acc (+)= X Y for X = [128 key][128 query] bf16 in TMEM (P^T or dS^T, at the
+// columns pds_col gives, + `sub` for dS^T) and Y = [128 query][d] in shared
+// memory (dO or Q) as an MN-major B operand: contraction over the queries.
 template <int D>
-__device__ __forceinline__ void mma_t(uint32_t tmem_d, uint32_t x, uint32_t y, bool accumulate) {
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t x_tmem, uint32_t y, bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    mma_f16_ss_elect(tmem_d, sdesc_sw128(x + kk * 2048, 16384, 1024), sdesc_sw128(y + kk * 2048, 16384, 1024),
-                     BwdCfg<D>::kIdescT, accumulate || kk > 0);
+    mma_f16_ts_elect(tmem_d, x_tmem + pds_col(kk), sdesc_sw128(y + kk * 2048, 16384, 1024), BwdCfg<D>::kIdescTS,
+                     accumulate || kk > 0);
   }
 }
 
-// dQ' = dS K_j: contraction over the keys; dS K-major, K_j ([key][d]) MN-major.
+// dQ' = dS K_j: contraction over the keys; the dS^T tile ([key][query]) read as an
+// MN-major A operand, K_j ([key][d]) as an MN-major B operand.
 template <int D>
-__device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint32_t ds, uint32_t k) {
+__device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint32_t ds_t, uint32_t k) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t byte = kk * 32;
-    const uint32_t off = (byte / 128) * 16384 + (byte % 128);
-    mma_f16_ss_elect(tmem_d, sdesc_sw128(ds + off, 16, 1024), sdesc_sw128(k + kk * 2048, 16384, 1024),
+    mma_f16_ss_elect(tmem_d, sdesc_sw128(ds_t + kk * 2048, 16384, 1024), sdesc_sw128(k + kk * 2048, 16384, 1024),
                      BwdCfg<D>::kIdescDQ, kk > 0);
   }
 }
 
-// D_i = sum_c dO_ic O_ic (fp32), and dQ accumulator rows zeroed.  One warp per row.
+// Per row of every head, padded to whole 128-row tiles: L * log2 e (+inf on
+// padding rows, so their P is 0) and D = sum_c dO_c O_c (0 on padding rows);
+// real rows of the dQ accumulator zeroed.  One warp per row.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, int n_pad) {
+  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(p.BH) * p.N) return;
+  if (prow >= static_cast<long long>(p.BH) * n_pad) return;
+  const int bh = static_cast<int>(prow / n_pad), r = static_cast<int>(prow % n_pad);
+  if (r >= p.N) {
+    if (lane == 0) {
+      p.lse2[prow] = INFINITY;
+      p.drow[prow] = 0.f;
+    }
+    return;
+  }
+  const long long row = static_cast<long long>(bh) * p.N + r;
   constexpr int kPer = D / 32;  // elements per lane (2 or 4)
   const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o) + row * D + lane * kPer;
   const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * kPer;
@@ -157,7 +218,10 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   for (int e = 0; e < kPer; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) p.drow[row] = acc;
+  if (lane == 0) {
+    p.drow[prow] = acc;
+    p.lse2[prow] = p.lse[row] * 1.4426950408889634f;
+  }
   float* dq = p.dq_acc + row * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) dq[e] = 0.f;
@@ -175,32 +239,81 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, lon
   }
 }
 
+// P^T and dS^T of one 32-query chunk of this thread's key row.  kMask: the
+// chunk needs the key mask (keys past N, or causal keys after the query).
+template <bool kMask>
+__device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], uint32_t l2_addr,
+                                           uint32_t d_addr, float sl2, int key_local, int q_local0, bool key_ok,
+                                           bool diag, uint32_t (&pw)[16], uint32_t (&dw)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 l2 = ld_shared_f4(l2_addr + 4 * c);
+    const float4 dr = ld_shared_f4(d_addr + 4 * c);
+    const float lv[4] = {l2.x, l2.y, l2.z, l2.w};
+    const float dv[4] = {dr.x, dr.y, dr.z, dr.w};
+    float pe[4], ds[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float e = ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lv[u]));
+      if (kMask) {
+        const bool keep = key_ok && (!diag || key_local <= q_local0 + c + u);
+        e = keep ? e : 0.f;
+      }
+      pe[u] = e;
+      ds[u] = e * (__uint_as_float(dp[c + u]) - dv[u]);
+    }
+    pw[c / 2] = pack_bf16x2(pe[0], pe[1]);
+    pw[c / 2 + 1] = pack_bf16x2(pe[2], pe[3]);
+    dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
+    dw[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+  }
+}
+
+// Grid n_kt * BH: CTA x takes key tile x / BH of head x % BH, so (causal) the
+// key tiles with the most query tiles start first.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  // The layout does not fit this base: report, touch nothing.
+  if (base + C::kUsed > raw + C::kSmemBytes) {
+    if (threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+    return;
+  }
   uint8_t* base_ptr = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBar);
-  const uint32_t kv_bar = smem_u32(bars), qd_bar = kv_bar + 8, mma1_bar = kv_bar + 16, mma2_bar = kv_bar + 24,
-                 done_bar = kv_bar + 32;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 5);
+  const uint32_t b0 = smem_u32(bars);
+  const uint32_t kv_bar = b0, s_full = b0 + 8, p_full = b0 + 16, dq_full = b0 + 24, drain_done = b0 + 32,
+                 fin_bar = b0 + 40;
+  auto q_full = [&](int s) { return b0 + 48 + 8 * s; };      // slot loaded
+  auto q_empty = [&](int s) { return b0 + 64 + 8 * s; };     // slot's Q, dO read by the MMAs
+  auto stage_free = [&](int s) { return b0 + 80 + 8 * s; };  // slot's dQ staged
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int N = p.N, n_kt = (N + 127) >> 7;
-  const int j = blockIdx.x, bh = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = p.N, n_kt = (N + 127) >> 7, n_pad = n_kt * 128;
+  const int j = static_cast<int>(blockIdx.x) / p.BH, bh = static_cast<int>(blockIdx.x) % p.BH;
+  const int i0 = kCausal ? j : 0;  // first query tile that sees key tile j
+  const int n_it = n_kt - i0;
   const uint64_t lim = p.timeout_ns;
 
   if (tid == 0) {
     mbar_init(kv_bar, 1);
-    mbar_init(qd_bar, 1);
-    mbar_init(mma1_bar, 1);
-    mbar_init(mma2_bar, 1);
-    mbar_init(done_bar, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(dq_full, 1);
+    mbar_init(drain_done, 8);
+    mbar_init(fin_bar, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1);
+      mbar_init(stage_free(s), 8);
+    }
     fence_mbarrier_init();
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
   }
@@ -208,164 +321,207 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t sK = base + C::kK, sV = base + C::kV, sQ = base + C::kQ, sDO = base + C::kDO;
-  const uint32_t sP = base + C::kP, sDS = base + C::kDS;
+  const uint32_t sK = base + C::kK, sV = base + C::kV, sDS = base + C::kDS;
+  auto sSlot = [&](int s) { return base + C::kSlot + s * C::kSlotBytes; };
+  auto sQ = [&](int s) { return sSlot(s); };
+  auto sDO = [&](int s) { return sSlot(s) + C::kTileBytes; };
+  auto sL2 = [&](int s) { return base + C::kL2 + s * 512; };
+  auto sDr = [&](int s) { return base + C::kDrow + s * 512; };
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
+    // ============================================================ TMA producer
     mbar_arrive_expect_tx_elect(kv_bar, 2 * C::kTileBytes);
     for (int b = 0; b < C::kBlocks; ++b) {
       tma_load_3d_elect(sK + b * 16384, &p.tm_k, kv_bar, b * 64, j * 128, bh);
       tma_load_3d_elect(sV + b * 16384, &p.tm_v, kv_bar, b * 64, j * 128, bh);
     }
-  }
-  bool ok = __syncthreads_and(mbar_wait(kv_bar, 0, p.status, lim));
-
-  const float sl2 = p.scale_log2;
-  const int key_r = j * 128 + tid;  // this thread's key row (dK, dV)
-  const int i0 = kCausal ? j : 0;   // first query tile that sees key tile j
-  // Q_i and dO_i of query tile i into shared memory (issued by warp 0).
-  auto load_qdo = [&](int i) {
-    mbar_arrive_expect_tx_elect(qd_bar, 2 * C::kTileBytes);
-    for (int b = 0; b < C::kBlocks; ++b) {
-      tma_load_3d_elect(sQ + b * 16384, &p.tm_q, qd_bar, b * 64, i * 128, bh);
-      tma_load_3d_elect(sDO + b * 16384, &p.tm_do, qd_bar, b * 64, i * 128, bh);
-    }
-  };
-  if (warp == 0) load_qdo(i0);
-  int it = 0;
-  for (int i = i0; ok && i < n_kt; ++i, ++it) {
-    const int row = i * 128 + tid;  // this thread's query row
-    // Rows past N: L = +inf makes every P of the row 0.
-    const float l2 = row < N ? p.lse[static_cast<size_t>(bh) * N + row] * 1.4426950408889634f : INFINITY;
-    const float drow = row < N ? p.drow[static_cast<size_t>(bh) * N + row] : 0.f;
-    ok = __syncthreads_and(mbar_wait(qd_bar, it & 1, p.status, lim));
-    if (!ok) break;
-    if (warp == 0) {
-      tc_fence_after();
-      mma_rows<D>(tmem + C::kColS, sQ, sK);
-      mma_rows<D>(tmem + C::kColDP, sDO, sV);
-      mma_commit_elect(mma1_bar);
-    }
-    // The previous tile's dQ reduce has read its staging copy (P and dS buffers).
-    if (tid == 0) bulk_wait_read_all();
-    ok = __syncthreads_and(mbar_wait(mma1_bar, it & 1, p.status, lim));
-    if (!ok) break;
-    tc_fence_after();
-    // P and dS of this thread's query row, 64 keys at a time (S and dP columns
-    // loaded together, one wait).
-#pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 64) {
-      uint32_t s[64], dp[64];
-      tmem_ld64x2_sync(tmem + lane_base + C::kColS + c0, s, tmem + lane_base + C::kColDP + c0, dp);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 32 * h + e + u;
-            const int key = j * 128 + c0 + c;
-            const bool keep = key < N && (!kCausal || key <= row);
-            const float pe = keep ? ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2)) : 0.f;
-            pv[u] = pe;
-            dv[u] = pe * (__uint_as_float(dp[c]) - drow);
-          }
-          pw[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          dw[e / 2] = pack_bf16x2(dv[0], dv[1]);
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int c = ((c0 + 32 * h) >> 3) + q4;  // 8-column chunk index 0..15
-          st_shared_v4(sw128_chunk(sP, tid, c), pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-          st_shared_v4(sw128_chunk(sDS, tid, c), dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
-        }
+    // dQ of query tile t, staged in its slot by the pass warps: reduce-add the
+    // boxes into the accumulator and wait until they are read, so the slot can
+    // be reloaded.
+    auto finish_tile = [&](int t) {
+      const int s = t & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), (t >> 1) & 1, p.status, lim, 64))) return false;
+      if (lane == 0) {
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, (i0 + t) * 128, bh);
+        bulk_commit_group();
+        bulk_wait_read_all();
       }
+      __syncwarp();
+      return true;
+    };
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1, i = i0 + it;
+      if (it >= 2) {  // the slot's previous query tile is read and its dQ reduced
+        ok = finish_tile(it - 2);
+        if (!ok) break;
+      }
+      mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
+      for (int b = 0; b < C::kBlocks; ++b) {
+        tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
+        tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
+      }
+      const size_t v0 = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
+      bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
+      bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
+      issued = it + 1;
     }
-    // The tensor core reads P and dS through the async proxy; S's columns are
-    // free for dS K once every thread has read them.
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
+    for (int t = n_it >= 2 ? n_it - 2 : 0; ok && t < n_it; ++t) ok = finish_tile(t);
+    if (lane == 0) bulk_wait_all();  // the dQ reduce-adds have completed
+    // Copies still in flight (only after a failed wait elsewhere) land before exit.
+    mbar_wait(kv_bar, 0, p.status, lim);
+    for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) mbar_wait(q_full(it & 1), (it >> 1) & 1, p.status, lim);
+  } else if (warp == kMmaWarp) {
+    // ============================================================ MMA issuer
+    bool ok = mbar_wait(kv_bar, 0, p.status, lim) && mbar_wait(q_full(0), 0, p.status, lim);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
       tc_fence_after();
-      mma_t<D>(tmem + C::kColDV, sP, sDO, it > 0);
-      mma_t<D>(tmem + C::kColDK, sDS, sQ, it > 0);
+      mma_rows<D>(tmem + C::kColS, sK, sQ(0));
+      mma_rows<D>(tmem + C::kColDP, sV, sDO(0));
+      mma_commit_elect(s_full);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(p_full, it & 1, p.status, lim));
+      if (!ok) break;
+      tc_fence_after();
+      mma_ts<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), it > 0);
+      mma_ts<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), it > 0);
+      mma_commit_elect(q_empty(s));
       mma_dq<D>(tmem + C::kColS, sDS, sK);
-      mma_commit_elect(mma2_bar);
+      mma_commit_elect(dq_full);
+      if (it + 1 < n_it) {
+        const int s1 = (it + 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), ((it + 1) >> 1) & 1, p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));
+        ok = __all_sync(0xffffffffu, mbar_wait(drain_done, it & 1, p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        mma_rows<D>(tmem + C::kColS, sK, sQ(s1));
+        mma_commit_elect(s_full);
+      }
     }
-    ok = __syncthreads_and(mbar_wait(mma2_bar, it & 1, p.status, lim));
-    if (!ok) break;
-    // Q_i and dO_i are read: the next query tile's copies overlap the dQ adds below.
-    if (warp == 0 && i + 1 < n_kt) load_qdo(i + 1);
-    tc_fence_after();
-    // dQ contribution scale * dS K_j: staged as fp32 in the P and dS buffers (no
-    // MMA reads them any more) in the 128-byte-swizzled layout of a 128-row x
-    // 32-float TMA box, then added to the fp32 accumulator by TMA reduce-adds,
-    // which clip the rows past N.  tcgen05.ld is warp-collective: every lane loads.
+    // Every MMA of this CTA completes before the epilogue reads dV, dK (and
+    // before TMEM is freed).
+    mma_commit_elect(fin_bar);
+    mbar_wait(fin_bar, 0, p.status, lim);
+  } else {
+    // ============================================================ pass / drain warps
+    const int qd = warp & 3, g = warp >> 2;
+    const int key_local = qd * 32 + lane;       // this thread's key row (TMEM lane)
+    const int key = j * 128 + key_local;
+    const bool key_ok = key < N;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1, i = i0 + it;
+      ok = pass_all(mbar_wait(s_full, it & 1, p.status, lim) && mbar_wait(q_full(s), (it >> 1) & 1, p.status, lim));
+      if (!ok) break;
+      tc_fence_after();
+      const bool diag = kCausal && i == j;
+      const bool mask = diag || !key_ok;
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t g[32];
-      tmem_ld32_sync(tmem + lane_base + C::kColS + c0, g);
-      const uint32_t blk = sP + (c0 / 32) * 16384 + tid * 128;
+      for (int q = 0; q < 2; ++q) {
+        const int col0 = 64 * g + 32 * q;  // first query (tile-local) of this chunk
+        uint32_t sv[32], dpv[32];
+        tmem_ld32x2_sync(tmem + lane_base + C::kColS + col0, sv, tmem + lane_base + C::kColDP + col0, dpv);
+        uint32_t pw[16], dw[16];
+        if (mask)
+          pass_chunk<true>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2, key_local, col0, key_ok, diag, pw, dw);
+        else
+          pass_chunk<false>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2, key_local, col0, key_ok, diag, pw, dw);
+        tmem_st16_sync(tmem + lane_base + C::kColDP + col0, pw);
+        tmem_st16_sync(tmem + lane_base + C::kColDP + col0 + 16, dw);
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4)
-        st_shared_v4(blk + ((q4 ^ (tid & 7)) << 4), __float_as_uint(__uint_as_float(g[4 * q4]) * p.scale),
-                     __float_as_uint(__uint_as_float(g[4 * q4 + 1]) * p.scale),
-                     __float_as_uint(__uint_as_float(g[4 * q4 + 2]) * p.scale),
-                     __float_as_uint(__uint_as_float(g[4 * q4 + 3]) * p.scale));
-    }
-    fence_proxy_async_smem();
-    // Next query tile: Q/dO and S/dP columns are reused.
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      for (int b = 0; b < D / 32; ++b) tma_reduce_add_3d(&p.tm_dqacc, sP + b * 16384, b * 32, i * 128, bh);
-      bulk_commit_group();
-    }
-  }
+        for (int c4 = 0; c4 < 4; ++c4)
+          st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + c4), dw[4 * c4], dw[4 * c4 + 1], dw[4 * c4 + 2],
+                       dw[4 * c4 + 3]);
+      }
+      // dS^T in shared memory is read by the tensor core (async proxy); P^T and
+      // dS^T in TMEM by the next MMAs.
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
 
-  if (ok) {
-    // Warp-collective TMEM loads by every lane; only key rows < N are stored.
-    tc_fence_after();
-    const size_t kr = static_cast<size_t>(bh) * N + (key_r < N ? key_r : 0);
-    __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
-    __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t a[32], b[32];
-      tmem_ld32_sync(tmem + lane_base + C::kColDV + c0, a);
-      tmem_ld32_sync(tmem + lane_base + C::kColDK + c0, b);
-      if (key_r >= N) continue;
+      // ---- drain dQ_i = dS K_j (S^T columns).  Warp w holds query rows 32 (w % 4)..
+      // and columns [g d/2, (g+1) d/2).  First out of TMEM (the next S^T may then
+      // be issued over it), then staged in this query tile's slot once its Q and
+      // dO are read; the producer warp reduce-adds the staged boxes.
+      ok = pass_all(mbar_wait(dq_full, it & 1, p.status, lim));
+      if (!ok) break;
+      tc_fence_after();
+      const int row_local = key_local;  // TMEM lane = query row of dQ_i
+      uint32_t gq[D / 2];
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        uint4 va, vb;
-        va.x = pack_bf16x2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-        va.y = pack_bf16x2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-        va.z = pack_bf16x2(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
-        va.w = pack_bf16x2(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
-        vb.x = pack_bf16x2(__uint_as_float(b[e]) * p.scale, __uint_as_float(b[e + 1]) * p.scale);
-        vb.y = pack_bf16x2(__uint_as_float(b[e + 2]) * p.scale, __uint_as_float(b[e + 3]) * p.scale);
-        vb.z = pack_bf16x2(__uint_as_float(b[e + 4]) * p.scale, __uint_as_float(b[e + 5]) * p.scale);
-        vb.w = pack_bf16x2(__uint_as_float(b[e + 6]) * p.scale, __uint_as_float(b[e + 7]) * p.scale);
-        *reinterpret_cast<uint4*>(dvp + c0 + e) = va;
-        *reinterpret_cast<uint4*>(dkp + c0 + e) = vb;
+      for (int c = 0; c < D / 2; c += 32)
+        tmem_ld32_sync(tmem + lane_base + C::kColS + g * (D / 2) + c, *reinterpret_cast<uint32_t(*)[32]>(gq + c));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(drain_done);
+      // Staging address of this thread's 16-byte chunk q4 of box b (row row_local).
+      const uint32_t stg = sSlot(s);
+      auto chunk_addr = [&](uint32_t slot_base, int b, int q4) {
+        return slot_base + b * 16384 + row_local * 128 + ((q4 ^ (row_local & 7)) << 4);
+      };
+      // The slot's Q and dO have been read (dV and dK were issued before dQ_i).
+      ok = pass_all(mbar_wait(q_empty(s), (it >> 1) & 1, p.status, lim));
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32)
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          st_shared_v4(chunk_addr(stg, (g * (D / 2) + c) / 32, q4),
+                       __float_as_uint(__uint_as_float(gq[c + 4 * q4]) * p.scale),
+                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 3]) * p.scale));
+      fence_proxy_async_smem();  // read by the producer's TMA reduce-adds
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stage_free(s));
+    }
+
+    // ---- epilogue: dK * scale and dV to bf16.  Warp-collective TMEM loads by
+    // every lane; only key rows < N are stored.
+    ok = pass_all(ok && mbar_wait(fin_bar, 0, p.status, lim));
+    if (ok) {
+      tc_fence_after();
+      const size_t kr = static_cast<size_t>(bh) * N + (key_ok ? key : 0);
+      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
+      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+#pragma unroll 1
+      for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32x2_sync(tmem + lane_base + C::kColDV + c0, a, tmem + lane_base + C::kColDK + c0, b);
+        if (!key_ok) continue;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 va, vb;
+          va.x = pack_bf16x2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+          va.y = pack_bf16x2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+          va.z = pack_bf16x2(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+          va.w = pack_bf16x2(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+          vb.x = pack_bf16x2(__uint_as_float(b[e]) * p.scale, __uint_as_float(b[e + 1]) * p.scale);
+          vb.y = pack_bf16x2(__uint_as_float(b[e + 2]) * p.scale, __uint_as_float(b[e + 3]) * p.scale);
+          vb.z = pack_bf16x2(__uint_as_float(b[e + 4]) * p.scale, __uint_as_float(b[e + 5]) * p.scale);
+          vb.w = pack_bf16x2(__uint_as_float(b[e + 6]) * p.scale, __uint_as_float(b[e + 7]) * p.scale);
+          *reinterpret_cast<uint4*>(dvp + c0 + e) = va;
+          *reinterpret_cast<uint4*>(dkp + c0 + e) = vb;
+        }
       }
     }
   }
 
-  // ---- teardown: the dQ reduce-adds have completed, every MMA of this CTA has
-  // completed before TMEM is freed
-  if (tid == 0) bulk_wait_all();
-  if (warp == 0) {
-    mma_commit_elect(done_bar);
-    mbar_wait(done_bar, 0, p.status, lim);
-  }
+  // ---- teardown: every role has finished with TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -376,9 +532,8 @@ cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   auto kern = attn_bwd_tc_kernel<D, kCausal>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int n_kt = (p.N + 127) / 128;
-  kern<<<dim3(static_cast<unsigned>(n_kt), static_cast<unsigned>(p.BH)), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes,
-         stream>>>(p);
+  const long long n_kt = (p.N + 127) / 128;
+  kern<<<static_cast<unsigned>(n_kt * p.BH), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -386,16 +541,17 @@ cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stream) {
   if (d != 64 && d != 128) return cudaErrorInvalidValue;
-  const long long rows = static_cast<long long>(p.BH) * p.N;
-  const unsigned prep_blocks = static_cast<unsigned>((rows + 7) / 8);
-  if (d == 128) attn_bwd_prep_kernel<128><<<prep_blocks, 256, 0, stream>>>(p);
-  else attn_bwd_prep_kernel<64><<<prep_blocks, 256, 0, stream>>>(p);
+  const int n_pad = (p.N + 127) / 128 * 128;
+  const long long prows = static_cast<long long>(p.BH) * n_pad;
+  const unsigned prep_blocks = static_cast<unsigned>((prows + 7) / 8);
+  if (d == 128) attn_bwd_prep_kernel<128><<<prep_blocks, 256, 0, stream>>>(p, n_pad);
+  else attn_bwd_prep_kernel<64><<<prep_blocks, 256, 0, stream>>>(p, n_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (d == 128) e = causal ? launch_main<128, true>(p, stream) : launch_main<128, false>(p, stream);
   else e = causal ? launch_main<64, true>(p, stream) : launch_main<64, false>(p, stream);
   if (e != cudaSuccess) return e;
-  const long long n4 = rows * d / 4;
+  const long long n4 = static_cast<long long>(p.BH) * p.N * d / 4;
   const long long want = (n4 + 255) / 256;
   const unsigned blocks = static_cast<unsigned>(want < 152LL * 16 ? want : 152LL * 16);
   attn_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(p, n4);
