@@ -170,15 +170,17 @@ __device__ __forceinline__ void mma_rows(uint32_t tmem_d, uint32_t a, uint32_t b
   }
 }
 
-// acc (+)= X Y for X = [128 key][128 query] bf16 in TMEM (P^T or dS^T, at the
-// columns pds_col gives, + `sub` for dS^T) and Y = [128 query][d] in shared
-// memory (dO or Q) as an MN-major B operand: contraction over the queries.
+// acc (+)= X Y over the queries of chunk q (k-steps kk with (kk >> 1) & 1 == q:
+// queries [32q, 32q + 32) and [64 + 32q, 96 + 32q)), for X = [128 key][128 query]
+// bf16 in TMEM (P^T or dS^T, at the columns pds_col gives, dS^T at + 16) and
+// Y = [128 query][d] in shared memory (dO or Q) as an MN-major B operand.
 template <int D>
-__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t x_tmem, uint32_t y, bool accumulate) {
+__device__ __forceinline__ void mma_ts_half(uint32_t tmem_d, uint32_t x_tmem, uint32_t y, int q, bool accumulate) {
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+  for (int h = 0; h < 4; ++h) {
+    const int kk = (h >> 1) * 4 + q * 2 + (h & 1);
     mma_f16_ts_elect(tmem_d, x_tmem + pds_col(kk), sdesc_sw128(y + kk * 2048, 16384, 1024), BwdCfg<D>::kIdescTS,
-                     accumulate || kk > 0);
+                     accumulate || h > 0);
   }
 }
 
@@ -193,9 +195,10 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint32_t ds_t, uint32_t 
   }
 }
 
-// Per row of every head, padded to whole 128-row tiles: L * log2 e (+inf on
-// padding rows, so their P is 0) and D = sum_c dO_c O_c (0 on padding rows);
-// real rows of the dQ accumulator zeroed.  One warp per row.
+// Per row of every head, padded to whole 128-row tiles: -L log2 e (-inf on
+// padding rows, so their P is 0) and -D with D = sum_c dO_c O_c (0 on padding
+// rows), negated so the pass adds them; real rows of the dQ accumulator zeroed.
+// One warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, int n_pad) {
   const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, i
   const int bh = static_cast<int>(prow / n_pad), r = static_cast<int>(prow % n_pad);
   if (r >= p.N) {
     if (lane == 0) {
-      p.lse2[prow] = INFINITY;
+      p.lse2[prow] = -INFINITY;
       p.drow[prow] = 0.f;
     }
     return;
@@ -219,8 +222,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, i
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    p.drow[prow] = acc;
-    p.lse2[prow] = p.lse[row] * 1.4426950408889634f;
+    p.drow[prow] = -acc;
+    p.lse2[prow] = -p.lse[row] * 1.4426950408889634f;
   }
   float* dq = p.dq_acc + row * D + lane * kPer;
 #pragma unroll
@@ -239,38 +242,39 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, lon
   }
 }
 
-// P^T and dS^T of one 32-query chunk of this thread's key row.  kMask: the
-// chunk needs the key mask (keys past N, or causal keys after the query).
+// P^T and dS^T of one 32-query chunk of this thread's key row, two queries per
+// packed f32x2 instruction: P = 2^(S sl2 + (-L log2 e)), dS = P (dP + (-D)).
+// kMask: the chunk needs the key mask (keys past N, or causal keys after the query).
 template <bool kMask>
-__device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], uint32_t l2_addr,
-                                           uint32_t d_addr, float sl2, int key_local, int q_local0, bool key_ok,
+__device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], uint32_t nl2_addr,
+                                           uint32_t nd_addr, uint64_t sl2x2, int key_local, int q_local0, bool key_ok,
                                            bool diag, uint32_t (&pw)[16], uint32_t (&dw)[16]) {
 #pragma unroll
   for (int c = 0; c < 32; c += 4) {
-    const float4 l2 = ld_shared_f4(l2_addr + 4 * c);
-    const float4 dr = ld_shared_f4(d_addr + 4 * c);
-    const float lv[4] = {l2.x, l2.y, l2.z, l2.w};
-    const float dv[4] = {dr.x, dr.y, dr.z, dr.w};
-    float pe[4], ds[4];
+    const float4 nl = ld_shared_f4(nl2_addr + 4 * c);
+    const float4 nd = ld_shared_f4(nd_addr + 4 * c);
+    const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, f2_pack(nl.x, nl.y));
+    const uint64_t x23 =
+        f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, f2_pack(nl.z, nl.w));
+    float e[4] = {ex2_approx(f2_lo(x01)), ex2_approx(f2_hi(x01)), ex2_approx(f2_lo(x23)), ex2_approx(f2_hi(x23))};
+    if (kMask) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float e = ex2_approx(fmaf(__uint_as_float(s[c + u]), sl2, -lv[u]));
-      if (kMask) {
+      for (int u = 0; u < 4; ++u) {
         const bool keep = key_ok && (!diag || key_local <= q_local0 + c + u);
-        e = keep ? e : 0.f;
+        e[u] = keep ? e[u] : 0.f;
       }
-      pe[u] = e;
-      ds[u] = e * (__uint_as_float(dp[c + u]) - dv[u]);
     }
-    pw[c / 2] = pack_bf16x2(pe[0], pe[1]);
-    pw[c / 2 + 1] = pack_bf16x2(pe[2], pe[3]);
-    dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
-    dw[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+    const uint64_t g01 = f2_add(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2_pack(nd.x, nd.y));
+    const uint64_t g23 = f2_add(f2_pack(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2_pack(nd.z, nd.w));
+    const uint64_t d01 = f2_mul(f2_pack(e[0], e[1]), g01);
+    const uint64_t d23 = f2_mul(f2_pack(e[2], e[3]), g23);
+    pw[c / 2] = pack_bf16x2(e[0], e[1]);
+    pw[c / 2 + 1] = pack_bf16x2(e[2], e[3]);
+    dw[c / 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
+    dw[c / 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
   }
 }
 
-// Grid n_kt * BH: CTA x takes key tile x / BH of head x % BH, so (causal) the
-// key tiles with the most query tiles start first.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -285,8 +289,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   uint8_t* base_ptr = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBar);
   const uint32_t b0 = smem_u32(bars);
-  const uint32_t kv_bar = b0, s_full = b0 + 8, p_full = b0 + 16, dq_full = b0 + 24, drain_done = b0 + 32,
-                 fin_bar = b0 + 40;
+  const uint32_t kv_bar = b0, s_full = b0 + 8, dq_full = b0 + 16, drain_done = b0 + 24, fin_bar = b0 + 32;
+  // P^T / dS^T chunk q (queries [32q, 32q + 32) and [64 + 32q, 96 + 32q)) written
+  auto p_full = [&](int q) { return b0 + 96 + 8 * q; };
   auto q_full = [&](int s) { return b0 + 48 + 8 * s; };      // slot loaded
   auto q_empty = [&](int s) { return b0 + 64 + 8 * s; };     // slot's Q, dO read by the MMAs
   auto stage_free = [&](int s) { return b0 + 80 + 8 * s; };  // slot's dQ staged
@@ -302,7 +307,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   if (tid == 0) {
     mbar_init(kv_bar, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, 8);
+    mbar_init(p_full(0), 8);
+    mbar_init(p_full(1), 8);
     mbar_init(dq_full, 1);
     mbar_init(drain_done, 8);
     mbar_init(fin_bar, 1);
@@ -385,11 +391,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     }
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(p_full, it & 1, p.status, lim));
+      // dV and dK over the queries of the first P^T / dS^T chunks while the pass
+      // computes the second ones.
+      ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), it & 1, p.status, lim));
       if (!ok) break;
       tc_fence_after();
-      mma_ts<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), it > 0);
-      mma_ts<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), it > 0);
+      mma_ts_half<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), 0, it > 0);
+      mma_ts_half<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), 0, it > 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(p_full(1), it & 1, p.status, lim));
+      if (!ok) break;
+      tc_fence_after();
+      mma_ts_half<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), 1, true);
+      mma_ts_half<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), 1, true);
       mma_commit_elect(q_empty(s));
       mma_dq<D>(tmem + C::kColS, sDS, sK);
       mma_commit_elect(dq_full);
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     const int key = j * 128 + key_local;
     const bool key_ok = key < N;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1, i = i0 + it;
@@ -433,22 +446,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         tmem_ld32x2_sync(tmem + lane_base + C::kColS + col0, sv, tmem + lane_base + C::kColDP + col0, dpv);
         uint32_t pw[16], dw[16];
         if (mask)
-          pass_chunk<true>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2, key_local, col0, key_ok, diag, pw, dw);
+          pass_chunk<true>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag, pw, dw);
         else
-          pass_chunk<false>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2, key_local, col0, key_ok, diag, pw, dw);
+          pass_chunk<false>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag, pw,
+                            dw);
         tmem_st16_sync(tmem + lane_base + C::kColDP + col0, pw);
         tmem_st16_sync(tmem + lane_base + C::kColDP + col0 + 16, dw);
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4)
           st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + c4), dw[4 * c4], dw[4 * c4 + 1], dw[4 * c4 + 2],
                        dw[4 * c4 + 3]);
+        // P^T and dS^T of this chunk in TMEM are read by dV and dK; dS^T in shared
+        // memory (async proxy) by dQ after the last chunk.
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(q));
       }
-      // dS^T in shared memory is read by the tensor core (async proxy); P^T and
-      // dS^T in TMEM by the next MMAs.
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
 
       // ---- drain dQ_i = dS K_j (S^T columns).  Warp w holds query rows 32 (w % 4)..
       // and columns [g d/2, (g+1) d/2).  First out of TMEM (the next S^T may then
