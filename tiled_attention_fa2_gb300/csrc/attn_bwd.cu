@@ -275,6 +275,11 @@ __device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32
   }
 }
 
+// Grid n_kt * BH.  Causal: CTA x takes key tile x / BH of head x % BH, so the key
+// tiles with the most query tiles start first.  Otherwise CTA x takes key tile
+// x % n_kt of head x / n_kt and visits the query tiles from its own index on
+// (cyclically): the CTAs of a head run together and reduce into different rows
+// of that head's dQ at any time, which keeps the accumulator in L2.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -299,9 +304,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, n_kt = (N + 127) >> 7, n_pad = n_kt * 128;
-  const int j = static_cast<int>(blockIdx.x) / p.BH, bh = static_cast<int>(blockIdx.x) % p.BH;
-  const int i0 = kCausal ? j : 0;  // first query tile that sees key tile j
-  const int n_it = n_kt - i0;
+  const int x = static_cast<int>(blockIdx.x);
+  const int j = kCausal ? x / p.BH : x % n_kt, bh = kCausal ? x % p.BH : x / n_kt;
+  const int n_it = kCausal ? n_kt - j : n_kt;  // causal: query tiles j .. n_kt - 1
+  // Query tile of this CTA's t-th step.
+  auto qtile = [&](int t) { return kCausal || j + t < n_kt ? j + t : j + t - n_kt; };
   const uint64_t lim = p.timeout_ns;
 
   if (tid == 0) {
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), (t >> 1) & 1, p.status, lim, 64))) return false;
       if (lane == 0) {
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, (i0 + t) * 128, bh);
+          tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, qtile(t) * 128, bh);
         bulk_commit_group();
         bulk_wait_read_all();
       }
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     int issued = 0;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1, i = i0 + it;
+      const int s = it & 1, i = qtile(it);
       if (it >= 2) {  // the slot's previous query tile is read and its dQ reduced
         ok = finish_tile(it - 2);
         if (!ok) break;
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it & 1, i = i0 + it;
+      const int s = it & 1, i = qtile(it);
       ok = pass_all(mbar_wait(s_full, it & 1, p.status, lim) && mbar_wait(q_full(s), (it >> 1) & 1, p.status, lim));
       if (!ok) break;
       tc_fence_after();
