@@ -195,6 +195,11 @@ __device__ __forceinline__ void mma_dq(uint32_t tmem_d, uint32_t ds_t, uint32_t 
   }
 }
 
+// Two bf16 (low half first) to floats.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
 // Per row of every head, padded to whole 128-row tiles: -L log2 e (-inf on
 // padding rows, so their P is 0) and -D with D = sum_c dO_c O_c (0 on padding
 // rows), negated so the pass adds them; real rows of the dQ accumulator zeroed.
@@ -213,21 +218,27 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, i
     return;
   }
   const long long row = static_cast<long long>(bh) * p.N + r;
-  constexpr int kPer = D / 32;  // elements per lane (2 or 4)
-  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o) + row * D + lane * kPer;
-  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * kPer;
+  // d / 32 elements per lane, moved with one vector access each.
   float acc = 0.f;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+  if constexpr (D == 128) {
+    const uint2 ov = reinterpret_cast<const uint2*>(p.o)[row * 32 + lane];
+    const uint2 gv = reinterpret_cast<const uint2*>(p.dout)[row * 32 + lane];
+    const float2 o0 = bf16x2_to_f2(ov.x), o1 = bf16x2_to_f2(ov.y), g0 = bf16x2_to_f2(gv.x), g1 = bf16x2_to_f2(gv.y);
+    acc = fmaf(o0.x, g0.x, fmaf(o0.y, g0.y, fmaf(o1.x, g1.x, o1.y * g1.y)));
+    reinterpret_cast<float4*>(p.dq_acc)[row * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    const uint32_t ov = reinterpret_cast<const uint32_t*>(p.o)[row * 32 + lane];
+    const uint32_t gv = reinterpret_cast<const uint32_t*>(p.dout)[row * 32 + lane];
+    const float2 o0 = bf16x2_to_f2(ov), g0 = bf16x2_to_f2(gv);
+    acc = fmaf(o0.x, g0.x, o0.y * g0.y);
+    reinterpret_cast<float2*>(p.dq_acc)[row * 32 + lane] = make_float2(0.f, 0.f);
+  }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
     p.drow[prow] = -acc;
     p.lse2[prow] = -p.lse[row] * 1.4426950408889634f;
   }
-  float* dq = p.dq_acc + row * D + lane * kPer;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) dq[e] = 0.f;
 }
 
 // dQ (bf16) = the fp32 accumulator, four elements per thread and step.
