@@ -25,7 +25,9 @@
 //              vectors into one of two slots, one query tile ahead; it also
 //              issues the dQ reduce-adds from the slots;
 //   warp 9     MMA issuer, per query tile i:
-//                dV += P^T dO_i, dK += dS^T Q_i   (A from TMEM; the last readers of the slot)
+//                dV += P^T dO_i, dK += dS^T Q_i   (A from TMEM; half of each once the
+//                                                   first 32-query chunks are written;
+//                                                   the last readers of the slot)
 //                dQ_i = dS K_j          (into the S^T columns, drained by warps 0-7)
 //                dP^T_{i+1} = V_j dO_{i+1}^T   (over P^T, dS^T: issued after their readers)
 //                S^T_{i+1} = K_j Q_{i+1}^T    (once the dQ_i drain has read its columns)
