@@ -54,20 +54,27 @@ template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile of Q, K, V or dO
   static constexpr int kBlocks = D / 64;          // 128-byte column blocks per row
-  // Shared memory (from a 1024-byte aligned base): K | V | slot 0 (Q, dO) | slot 1 (Q, dO)
-  // | dS^T | L2 slot 0, 1 | D slot 0, 1 | barriers.  A slot, once its Q and dO are
-  // read, stages that query tile's fp32 dQ (128 x d x 4 bytes = the slot's size)
-  // as d/32 TMA boxes of 128 rows x 32 floats.
+  // d = 64 leaves room for a third Q/dO slot in shared memory and a second S^T
+  // buffer in TMEM: the next query tile's S^T is then computed during the current
+  // pass, and the next pass does not wait for the dQ drain.
+  static constexpr bool kDblS = (D == 64);
+  static constexpr int kSlots = kDblS ? 3 : 2;
+  // Shared memory (from a 1024-byte aligned base): K | V | slots (Q, dO) | dS^T |
+  // L2 per slot | D per slot | barriers.  A slot, once its Q and dO are read,
+  // stages that query tile's fp32 dQ (128 x d x 4 bytes = the slot's size) as
+  // d/32 TMA boxes of 128 rows x 32 floats.
   static constexpr int kK = 0, kV = kTileBytes, kSlot = 2 * kTileBytes, kSlotBytes = 2 * kTileBytes;
-  static constexpr int kDS = 6 * kTileBytes;
+  static constexpr int kDS = kSlot + kSlots * kSlotBytes;
   static constexpr int kBoxes = D / 32;  // dQ staging boxes per query tile
-  static constexpr int kL2 = kDS + kPSBytes, kDrow = kL2 + 2 * 512;
-  static constexpr int kBar = kDrow + 2 * 512;
+  static constexpr int kL2 = kDS + kPSBytes, kDrow = kL2 + kSlots * 512;
+  static constexpr int kBar = kDrow + kSlots * 512;
   static constexpr int kUsed = kBar + 16 * 8 + 16;
   static constexpr int kSmemBytes = (kUsed + 1024 < kMaxSmem) ? kUsed + 1024 : kMaxSmem;
   static_assert(kUsed <= kMaxSmem, "shared memory layout too large");
-  // TMEM columns: dV | dK | S^T (then dQ) | dP^T (then P^T and dS^T, bf16)
-  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  // TMEM columns: dV | dK | S^T (then dQ; two buffers when kDblS) | dP^T (then P^T
+  // and dS^T, bf16)
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + (kDblS ? 256 : 128);
+  static_assert(kColDP + 128 <= 512, "TMEM columns");
   static constexpr uint32_t kIdescQK = make_idesc(1, 128, 128, 0, 0);  // S^T, dP^T: both operands K-major
   static constexpr uint32_t kIdescTS = make_idesc(1, 128, D, 0, 1);    // dV, dK: A in TMEM, B = dO / Q MN-major
   static constexpr uint32_t kIdescDQ = make_idesc(1, 128, D, 1, 1);    // dS K: A = dS^T tile MN-major, B = K MN-major
@@ -309,10 +316,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   const uint32_t b0 = smem_u32(bars);
   const uint32_t kv_bar = b0, s_full = b0 + 8, dq_full = b0 + 16, drain_done = b0 + 24, fin_bar = b0 + 32;
   // P^T / dS^T chunk q (queries [32q, 32q + 32) and [64 + 32q, 96 + 32q)) written
-  auto p_full = [&](int q) { return b0 + 96 + 8 * q; };
-  auto q_full = [&](int s) { return b0 + 48 + 8 * s; };      // slot loaded
-  auto q_empty = [&](int s) { return b0 + 64 + 8 * s; };     // slot's Q, dO read by the MMAs
-  auto stage_free = [&](int s) { return b0 + 80 + 8 * s; };  // slot's dQ staged
+  auto p_full = [&](int q) { return b0 + 40 + 8 * q; };
+  auto q_full = [&](int s) { return b0 + 56 + 8 * s; };       // slot loaded
+  auto q_empty = [&](int s) { return b0 + 80 + 8 * s; };      // slot's Q, dO read by the MMAs
+  auto stage_free = [&](int s) { return b0 + 104 + 8 * s; };  // slot's dQ staged
+  // Query tile t uses slot t % kSlots for the (t / kSlots)-th time.
+  constexpr int kSl = C::kSlots;
+  auto slot_of = [](int t) { return t % kSl; };
+  auto use_par = [](int t) { return static_cast<uint32_t>((t / kSl) & 1); };
+  // S^T (then dQ) columns of query tile t.
+  auto col_s = [](int t) { return C::kColS + (C::kDblS ? 128u * static_cast<uint32_t>(t & 1) : 0u); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -332,7 +345,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     mbar_init(dq_full, 1);
     mbar_init(drain_done, 8);
     mbar_init(fin_bar, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSl; ++s) {
       mbar_init(q_full(s), 1);
       mbar_init(q_empty(s), 1);
       mbar_init(stage_free(s), 8);
@@ -365,8 +378,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     // boxes into the accumulator and wait until they are read, so the slot can
     // be reloaded.
     auto finish_tile = [&](int t) {
-      const int s = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), (t >> 1) & 1, p.status, lim, 64))) return false;
+      const int s = slot_of(t);
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), use_par(t), p.status, lim, 64))) return false;
       if (lane == 0) {
         for (int b = 0; b < C::kBoxes; ++b)
           tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, qtile(t) * 128, bh);
@@ -379,9 +392,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     int issued = 0;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1, i = qtile(it);
-      if (it >= 2) {  // the slot's previous query tile is read and its dQ reduced
-        ok = finish_tile(it - 2);
+      const int s = slot_of(it), i = qtile(it);
+      if (it >= kSl) {  // the slot's previous query tile is read and its dQ reduced
+        ok = finish_tile(it - kSl);
         if (!ok) break;
       }
       mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
@@ -394,23 +407,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
       issued = it + 1;
     }
-    for (int t = n_it >= 2 ? n_it - 2 : 0; ok && t < n_it; ++t) ok = finish_tile(t);
+    for (int t = n_it >= kSl ? n_it - kSl : 0; ok && t < n_it; ++t) ok = finish_tile(t);
     if (lane == 0) bulk_wait_all();  // the dQ reduce-adds have completed
     // Copies still in flight (only after a failed wait elsewhere) land before exit.
     mbar_wait(kv_bar, 0, p.status, lim);
-    for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) mbar_wait(q_full(it & 1), (it >> 1) & 1, p.status, lim);
+    for (int it = issued > kSl ? issued - kSl : 0; it < issued; ++it)
+      mbar_wait(q_full(slot_of(it)), use_par(it), p.status, lim);
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
     bool ok = mbar_wait(kv_bar, 0, p.status, lim) && mbar_wait(q_full(0), 0, p.status, lim);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      mma_rows<D>(tmem + C::kColS, sK, sQ(0));
+      mma_rows<D>(tmem + col_s(0), sK, sQ(0));
       mma_rows<D>(tmem + C::kColDP, sV, sDO(0));
       mma_commit_elect(s_full);
     }
     for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it & 1;
+      const int s = slot_of(it);
+      if (C::kDblS && it + 1 < n_it) {
+        // The next query tile's S^T into the other buffer, to run during this
+        // pass, once that buffer's dQ (query tile it - 1) is out of TMEM.
+        const int s1 = slot_of(it + 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(it + 1), p.status, lim) &&
+                                         (it == 0 || mbar_wait(drain_done, (it - 1) & 1, p.status, lim)));
+        if (!ok) break;
+        tc_fence_after();
+        mma_rows<D>(tmem + col_s(it + 1), sK, sQ(s1));
+      }
       // dV and dK over the queries of the first P^T / dS^T chunks while the pass
       // computes the second ones.
       ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), it & 1, p.status, lim));
@@ -424,18 +448,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       mma_ts_half<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), 1, true);
       mma_ts_half<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), 1, true);
       mma_commit_elect(q_empty(s));
-      mma_dq<D>(tmem + C::kColS, sDS, sK);
+      mma_dq<D>(tmem + col_s(it), sDS, sK);
       mma_commit_elect(dq_full);
       if (it + 1 < n_it) {
-        const int s1 = (it + 1) & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), ((it + 1) >> 1) & 1, p.status, lim));
-        if (!ok) break;
-        tc_fence_after();
-        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));
-        ok = __all_sync(0xffffffffu, mbar_wait(drain_done, it & 1, p.status, lim));
-        if (!ok) break;
-        tc_fence_after();
-        mma_rows<D>(tmem + C::kColS, sK, sQ(s1));
+        const int s1 = slot_of(it + 1);
+        if (!C::kDblS) {
+          ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(it + 1), p.status, lim));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));  // over P^T, dS^T: issued after their readers
+        if (!C::kDblS) {
+          ok = __all_sync(0xffffffffu, mbar_wait(drain_done, it & 1, p.status, lim));
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows<D>(tmem + col_s(it + 1), sK, sQ(s1));
+        }
         mma_commit_elect(s_full);
       }
     }
@@ -453,8 +481,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it & 1, i = qtile(it);
-      ok = pass_all(mbar_wait(s_full, it & 1, p.status, lim) && mbar_wait(q_full(s), (it >> 1) & 1, p.status, lim));
+      const int s = slot_of(it), i = qtile(it);
+      ok = pass_all(mbar_wait(s_full, it & 1, p.status, lim) && mbar_wait(q_full(s), use_par(it), p.status, lim));
       if (!ok) break;
       tc_fence_after();
       const bool diag = kCausal && i == j;
@@ -463,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       for (int q = 0; q < 2; ++q) {
         const int col0 = 64 * g + 32 * q;  // first query (tile-local) of this chunk
         uint32_t sv[32], dpv[32];
-        tmem_ld32x2_sync(tmem + lane_base + C::kColS + col0, sv, tmem + lane_base + C::kColDP + col0, dpv);
+        tmem_ld32x2_sync(tmem + lane_base + col_s(it) + col0, sv, tmem + lane_base + C::kColDP + col0, dpv);
         uint32_t pw[16], dw[16];
         if (mask)
           pass_chunk<true>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag, pw, dw);
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       uint32_t gq[D / 2];
 #pragma unroll
       for (int c = 0; c < D / 2; c += 32)
-        tmem_ld32_sync(tmem + lane_base + C::kColS + g * (D / 2) + c, *reinterpret_cast<uint32_t(*)[32]>(gq + c));
+        tmem_ld32_sync(tmem + lane_base + col_s(it) + g * (D / 2) + c, *reinterpret_cast<uint32_t(*)[32]>(gq + c));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(drain_done);
@@ -505,7 +533,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         return slot_base + b * 16384 + row_local * 128 + ((q4 ^ (row_local & 7)) << 4);
       };
       // The slot's Q and dO have been read (dV and dK were issued before dQ_i).
-      ok = pass_all(mbar_wait(q_empty(s), (it >> 1) & 1, p.status, lim));
+      ok = pass_all(mbar_wait(q_empty(s), use_par(it), p.status, lim));
       if (!ok) break;
 #pragma unroll
       for (int c = 0; c < D / 2; c += 32)
