@@ -80,11 +80,11 @@ struct BwdCfg {
   static constexpr uint32_t kIdescDQ = make_idesc(1, 128, D, 1, 1);    // dS K: A = dS^T tile MN-major, B = K MN-major
 };
 
-// TMEM column (relative to the dP^T block) of the bf16 P^T (dS^T: + 16) values
-// of queries [16 kk, 16 kk + 16): pass warpgroup g writes queries [64g, 64g + 64)
-// in two 32-query chunks, each chunk's P^T then dS^T over the 32 dP^T columns it
-// has just read.
-__device__ __forceinline__ uint32_t pds_col(int kk) { return (kk >> 2) * 64 + ((kk >> 1) & 1) * 32 + (kk & 1) * 8; }
+// TMEM column (relative to the S^T block) of the bf16 P^T values of queries
+// [16 kk, 16 kk + 16); their dS^T follow at + 8.  The pass writes each 16-query
+// group over the 16 S^T columns it has just read, so later groups' S^T (and all
+// of dP^T) stay intact while their loads are in flight.
+__device__ __forceinline__ uint32_t pds_col(int kk) { return 16u * static_cast<uint32_t>(kk); }
 
 // Bulk tensor reduce-add shared -> global (element type and box from the map),
 // tracked by the issuing thread's bulk async-groups.
@@ -181,7 +181,7 @@ __device__ __forceinline__ void mma_rows(uint32_t tmem_d, uint32_t a, uint32_t b
 
 // acc (+)= X Y over the queries of chunk q (k-steps kk with (kk >> 1) & 1 == q:
 // queries [32q, 32q + 32) and [64 + 32q, 96 + 32q)), for X = [128 key][128 query]
-// bf16 in TMEM (P^T or dS^T, at the columns pds_col gives, dS^T at + 16) and
+// bf16 in TMEM (P^T or dS^T, at the columns pds_col gives, dS^T at + 8) and
 // Y = [128 query][d] in shared memory (dO or Q) as an MN-major B operand.
 template <int D>
 __device__ __forceinline__ void mma_ts_half(uint32_t tmem_d, uint32_t x_tmem, uint32_t y, int q, bool accumulate) {
@@ -262,15 +262,16 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, lon
   }
 }
 
-// P^T and dS^T of one 32-query chunk of this thread's key row, two queries per
-// packed f32x2 instruction: P = 2^(S sl2 + (-L log2 e)), dS = P (dP + (-D)).
-// kMask: the chunk needs the key mask (keys past N, or causal keys after the query).
+// P^T and dS^T of one 16-query group of this thread's key row, two queries per
+// packed f32x2 instruction: P = 2^(S sl2 + (-L log2 e)), dS = P (dP + (-D)); 8
+// packed P^T and 8 packed dS^T words out.  kMask: the group needs the key mask
+// (keys past N, or causal keys after the query).
 template <bool kMask>
-__device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], uint32_t nl2_addr,
+__device__ __forceinline__ void pass_sub16(const uint32_t (&s)[16], const uint32_t (&dp)[16], uint32_t nl2_addr,
                                            uint32_t nd_addr, uint64_t sl2x2, int key_local, int q_local0, bool key_ok,
-                                           bool diag, uint32_t (&pw)[16], uint32_t (&dw)[16]) {
+                                           bool diag, uint32_t (&pw)[8], uint32_t (&dw)[8]) {
 #pragma unroll
-  for (int c = 0; c < 32; c += 4) {
+  for (int c = 0; c < 16; c += 4) {
     const float4 nl = ld_shared_f4(nl2_addr + 4 * c);
     const float4 nd = ld_shared_f4(nd_addr + 4 * c);
     const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, f2_pack(nl.x, nl.y));
@@ -295,11 +296,42 @@ __device__ __forceinline__ void pass_chunk(const uint32_t (&s)[32], const uint32
   }
 }
 
-// Grid n_kt * BH.  Causal: CTA x takes key tile x / BH of head x % BH, so the key
-// tiles with the most query tiles start first.  Otherwise CTA x takes key tile
-// x % n_kt of head x / n_kt and visits the query tiles from its own index on
-// (cyclically): the CTAs of a head run together and reduce into different rows
-// of that head's dQ at any time, which keeps the accumulator in L2.
+// Two 32-lane x 16-column TMEM loads issued without waiting; their registers
+// become usable only through tmem_wait_ld16x2 below.
+__device__ __forceinline__ void tmem_ld16x2_issue(uint32_t ta, uint32_t (&a)[16], uint32_t tb, uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]),
+        "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(b[0]),
+        "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]),
+        "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+// Waits for every TMEM load of this thread; the registers pass through the
+// statement, so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld16x2(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),
+                 "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
+                 "+r"(b[14]), "+r"(b[15])
+               :
+               : "memory");
+}
+// Two 32-lane x 8-column TMEM stores, not waited for (tmem_wait_st does).
+__device__ __forceinline__ void tmem_st8x2_issue(uint32_t ta, const uint32_t (&a)[8], uint32_t tb, const uint32_t (&b)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9};\n"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(ta),
+      "r"(tb), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(b[0]),
+      "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -440,13 +472,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), it & 1, p.status, lim));
       if (!ok) break;
       tc_fence_after();
-      mma_ts_half<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), 0, it > 0);
-      mma_ts_half<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), 0, it > 0);
+      mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(it), sDO(s), 0, it > 0);
+      mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(it) + 8, sQ(s), 0, it > 0);
       ok = __all_sync(0xffffffffu, mbar_wait(p_full(1), it & 1, p.status, lim));
       if (!ok) break;
       tc_fence_after();
-      mma_ts_half<D>(tmem + C::kColDV, tmem + C::kColDP, sDO(s), 1, true);
-      mma_ts_half<D>(tmem + C::kColDK, tmem + C::kColDP + 16, sQ(s), 1, true);
+      mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(it), sDO(s), 1, true);
+      mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(it) + 8, sQ(s), 1, true);
       mma_commit_elect(q_empty(s));
       mma_dq<D>(tmem + col_s(it), sDS, sK);
       mma_commit_elect(dq_full);
@@ -457,7 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
           if (!ok) break;
           tc_fence_after();
         }
-        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));  // over P^T, dS^T: issued after their readers
+        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));  // the pass has read dP^T
         if (!C::kDblS) {
           ok = __all_sync(0xffffffffu, mbar_wait(drain_done, it & 1, p.status, lim));
           if (!ok) break;
@@ -487,29 +519,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       tc_fence_after();
       const bool diag = kCausal && i == j;
       const bool mask = diag || !key_ok;
-#pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
-        const int col0 = 64 * g + 32 * q;  // first query (tile-local) of this chunk
-        uint32_t sv[32], dpv[32];
-        tmem_ld32x2_sync(tmem + lane_base + col_s(it) + col0, sv, tmem + lane_base + C::kColDP + col0, dpv);
-        uint32_t pw[16], dw[16];
-        if (mask)
-          pass_chunk<true>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag, pw, dw);
-        else
-          pass_chunk<false>(sv, dpv, sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag, pw,
-                            dw);
-        tmem_st16_sync(tmem + lane_base + C::kColDP + col0, pw);
-        tmem_st16_sync(tmem + lane_base + C::kColDP + col0 + 16, dw);
+      // Four 16-query groups (queries 64g + 16u ..): group u + 1's S^T and dP^T
+      // loads are in flight while group u is computed; P^T and dS^T go over the
+      // group's own S^T columns.  After groups 1 and 3 (a 32-query chunk) the
+      // stores are waited for and the chunk is handed to the MMA warp.
+      uint32_t sv[2][16], dpv[2][16];
+      tmem_ld16x2_issue(tmem + lane_base + col_s(it) + 64 * g, sv[0], tmem + lane_base + C::kColDP + 64 * g, dpv[0]);
+      tmem_wait_ld16x2(sv[0], dpv[0]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + c4), dw[4 * c4], dw[4 * c4 + 1], dw[4 * c4 + 2],
-                       dw[4 * c4 + 3]);
-        // P^T and dS^T of this chunk in TMEM are read by dV and dK; dS^T in shared
-        // memory (async proxy) by dQ after the last chunk.
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(q));
+      for (int u = 0; u < 4; ++u) {
+        const int b = u & 1;
+        const int col0 = 64 * g + 16 * u;  // first query (tile-local) of this group
+        if (u < 3)
+          tmem_ld16x2_issue(tmem + lane_base + col_s(it) + col0 + 16, sv[b ^ 1],
+                            tmem + lane_base + C::kColDP + col0 + 16, dpv[b ^ 1]);
+        uint32_t pw[8], dw[8];
+        if (mask)
+          pass_sub16<true>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
+                           pw, dw);
+        else
+          pass_sub16<false>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
+                            pw, dw);
+        tmem_st8x2_issue(tmem + lane_base + col_s(it) + col0, pw, tmem + lane_base + col_s(it) + col0 + 8, dw);
+        st_shared_v4(sw128_chunk(sDS, key_local, col0 >> 3), dw[0], dw[1], dw[2], dw[3]);
+        st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + 1), dw[4], dw[5], dw[6], dw[7]);
+        if (u & 1) {
+          // P^T and dS^T of this chunk in TMEM are read by dV and dK; dS^T in
+          // shared memory (async proxy) by dQ after the last chunk.
+          tmem_wait_st();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full(u >> 1));
+        }
+        if (u < 3) tmem_wait_ld16x2(sv[b ^ 1], dpv[b ^ 1]);
       }
 
       // ---- drain dQ_i = dS K_j (S^T columns).  Warp w holds query rows 32 (w % 4)..
