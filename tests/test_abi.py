@@ -81,6 +81,13 @@ def test_host_entry_validates_before_copying(lib):
     st = lib.attn_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                            1, 1, 128, 64, 0.1, 1.0, 1.0, 1.0, 0, 9, None)
     assert st == 1
+    # What only the kernel of the dtype requires is checked before the copies
+    # too: an unsupported head dimension or an o that the bf16 kernel cannot
+    # store to (32-byte rule) returns its own status, not a failed copy.
+    for d, dtype, d_o, want in ((96, 1, FAKE, 2), (64, 2, FAKE, 2), (48, 0, FAKE, 2), (128, 1, FAKE + 16, 3)):
+        st = lib.attn_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, d_o, FAKE,
+                               1, 1, 128, d, 0.1, 1.0, 1.0, 1.0, 0, dtype, None)
+        assert st == want, (d, dtype, st, lib.attn_last_error())
 
 
 def test_wait_limit_setter_round_trips(lib):

@@ -217,10 +217,35 @@ int run_f32(const void* q, const void* k, const void* v, void* o, float* lse, in
   return ATTN_OK;
 }
 
+// The requirements of the kernel that serves `dtype` (head dimension, output
+// alignment, grid size), checked without launching anything; run_tc and
+// run_f32 check the same before their launches.
+int check_kernel(const void* o, int B, int H, int N, int d, int dtype) {
+  switch (dtype) {
+    case ATTN_F32:
+      if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "fp32 path supports d in {16, 32, 64, 128} (got %d)", d);
+      return ATTN_OK;
+    case ATTN_BF16:
+    case ATTN_E4M3: {
+      const bool fp8 = dtype == ATTN_E4M3;
+      if (fp8 ? (d != 128) : (d != 64 && d != 128))
+        return fail(ATTN_ERR_UNSUPPORTED, "%s tensor-core path supports d in %s (got %d)", fp8 ? "e4m3" : "bf16",
+                    fp8 ? "{128}" : "{64, 128}", d);
+      if (!aligned(o, 32)) return fail(ATTN_ERR_MISALIGNED, "o must be 32-byte aligned for bf16/e4m3 inputs");
+      const long long n_pairs = (static_cast<long long>(N) + 255) / 256;
+      if (n_pairs * B * H > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "grid too large (B*H*ceil(N/256))");
+      return ATTN_OK;
+    }
+    default: return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  }
+}
+
 int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              float scale, float qds, float kds, float vds, int causal, int dtype, cudaStream_t stream) {
   int st = check_common(q, k, v, o, lse, B, H, N, d, scale, causal);
   if (st != ATTN_OK) return st;
+  if ((st = check_kernel(o, B, H, N, d, dtype)) != ATTN_OK) return st;
   switch (dtype) {
     case ATTN_F32: return run_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream);
     case ATTN_BF16: return run_tc(q, k, v, o, lse, B, H, N, d, scale, 1.f, 1.f, 1.f, causal, false, stream);
@@ -280,6 +305,8 @@ int attn_fwd_host(const void* h_q, const void* h_k, const void* h_v, void* h_o, 
     return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
   if (dtype == ATTN_E4M3 && (!good_descale(q_descale) || !good_descale(k_descale) || !good_descale(v_descale)))
     return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
+  // Everything the forward would reject is rejected before the first copy is enqueued.
+  if ((st = check_kernel(d_o, B, H, N, d, dtype)) != ATTN_OK) return st;
   const size_t in_elem = dtype == ATTN_F32 ? 4 : (dtype == ATTN_BF16 ? 2 : 1);
   const size_t out_elem = dtype == ATTN_F32 ? 4 : 2;
   const size_t rows = static_cast<size_t>(B) * H * N;
