@@ -97,7 +97,20 @@ def _shape(q, k, v):
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError(f"q, k, v must be on one device (got {q.device}, {k.device}, {v.device})")
     return tuple(int(x) for x in q.shape)
+
+
+def _require(name, t, device, dtype, shape):
+    """A buffer the library reads or writes: a contiguous CUDA tensor of the
+    given dtype and shape on `device` (a host tensor here would hand the kernel
+    a host address)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"(got {t.dtype} {tuple(t.shape)})")
 
 
 def _outputs(q, o, lse, B, H, N, d, code):
@@ -106,10 +119,8 @@ def _outputs(q, o, lse, B, H, N, d, code):
         o = torch.empty((B, H, N, d), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if o.dtype != odt or tuple(o.shape) != (B, H, N, d) or not o.is_contiguous():
-        raise ValueError(f"o must be a contiguous {odt} tensor of shape {(B, H, N, d)}")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
-        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(B, H, N)}")
+    _require("o", o, q.device, odt, (B, H, N, d))
+    _require("lse", lse, q.device, torch.float32, (B, H, N))
     return o, lse
 
 
@@ -121,8 +132,9 @@ def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
     o, lse = _outputs(q, o, lse, B, H, N, d, code)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     lib = load_library()
-    _check(lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                        scale, int(bool(causal)), code, _stream_handle(stream, q.device)))
+    with torch.cuda.device(q.device):
+        _check(lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                            scale, int(bool(causal)), code, _stream_handle(stream, q.device)))
     return o, lse
 
 
@@ -136,9 +148,10 @@ def attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, sca
     o, lse = _outputs(q, o, lse, B, H, N, d, ATTN_E4M3)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     lib = load_library()
-    _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                            scale, float(q_descale), float(k_descale), float(v_descale), int(bool(causal)),
-                            _stream_handle(stream, q.device)))
+    with torch.cuda.device(q.device):
+        _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,
+                                d, scale, float(q_descale), float(k_descale), float(v_descale), int(bool(causal)),
+                                _stream_handle(stream, q.device)))
     return o, lse
 
 
@@ -147,20 +160,35 @@ def attn_fwd_host(h_q, h_k, h_v, h_o, h_lse, d_q, d_k, d_v, d_o, d_lse, scale=No
     """End-to-end forward from (page-locked) host tensors through caller-owned
     device staging tensors: H2D copies, forward, D2H copies, all enqueued on
     `stream`.  The caller synchronises before reading h_o / h_lse."""
+    if h_q.dim() != 4:
+        raise ValueError(f"h_q must be [B, H, N, d] (got shape {tuple(h_q.shape)})")
     B, H, N, d = (int(x) for x in h_q.shape)
     code = _dtype_code(h_q)
-    for t in (d_q, d_k, d_v, d_o, d_lse):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("device staging tensors must be contiguous CUDA tensors")
-    for t in (h_q, h_k, h_v, h_o, h_lse):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("host tensors must be contiguous CPU tensors")
+    odt = torch.float32 if code == ATTN_F32 else torch.bfloat16
+    # Every copy moves the bytes of [B, H, N, d] (or [B, H, N]) elements, so each
+    # buffer must hold exactly that many of its dtype.
+    want = {"h_q": (h_q, h_q.dtype, (B, H, N, d)), "h_k": (h_k, h_q.dtype, (B, H, N, d)),
+            "h_v": (h_v, h_q.dtype, (B, H, N, d)), "h_o": (h_o, odt, (B, H, N, d)),
+            "h_lse": (h_lse, torch.float32, (B, H, N))}
+    for name, (t, dt, shape) in want.items():
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+        if t.dtype != dt or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a {dt} tensor of shape {shape} (got {t.dtype} {tuple(t.shape)})")
+    if not isinstance(d_q, torch.Tensor) or not d_q.is_cuda:
+        raise ValueError("d_q must be a CUDA tensor")
+    dev = d_q.device
+    for name, t in (("d_q", d_q), ("d_k", d_k), ("d_v", d_v)):
+        _require(name, t, dev, h_q.dtype, (B, H, N, d))
+    _require("d_o", d_o, dev, odt, (B, H, N, d))
+    _require("d_lse", d_lse, dev, torch.float32, (B, H, N))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     lib = load_library()
-    _check(lib.attn_fwd_host(h_q.data_ptr(), h_k.data_ptr(), h_v.data_ptr(), h_o.data_ptr(), h_lse.data_ptr(),
-                             d_q.data_ptr(), d_k.data_ptr(), d_v.data_ptr(), d_o.data_ptr(), d_lse.data_ptr(),
-                             B, H, N, d, scale, float(descales[0]), float(descales[1]), float(descales[2]),
-                             int(bool(causal)), code, _stream_handle(stream, d_q.device)))
+    with torch.cuda.device(dev):
+        _check(lib.attn_fwd_host(h_q.data_ptr(), h_k.data_ptr(), h_v.data_ptr(), h_o.data_ptr(), h_lse.data_ptr(),
+                                 d_q.data_ptr(), d_k.data_ptr(), d_v.data_ptr(), d_o.data_ptr(), d_lse.data_ptr(),
+                                 B, H, N, d, scale, float(descales[0]), float(descales[1]), float(descales[2]),
+                                 int(bool(causal)), code, _stream_handle(stream, dev)))
 
 
 def split_plan(B, H, N, d, n_splits=0):
@@ -179,15 +207,19 @@ def attn_fwd_split(q, k, v, n_splits=0, descales=None, o=None, lse=None, scale=N
     code = _dtype_code(q)
     o, lse = _outputs(q, o, lse, B, H, N, d, code)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    _, nbytes = split_plan(B, H, N, d, n_splits)
+    with torch.cuda.device(q.device):
+        _, nbytes = split_plan(B, H, N, d, n_splits)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {q.device}")
     ds = descales if descales is not None else (1.0, 1.0, 1.0)
     lib = load_library()
-    _check(lib.attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                              scale, float(ds[0]), float(ds[1]), float(ds[2]), 0, code, int(n_splits),
-                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                              _stream_handle(stream, q.device)))
+    with torch.cuda.device(q.device):
+        _check(lib.attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,
+                                  d, scale, float(ds[0]), float(ds[1]), float(ds[2]), 0, code, int(n_splits),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, q.device)))
     return o, lse
 
 
@@ -206,23 +238,27 @@ def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale=None, causa
     B, H, N, d = _shape(q, k, v)
     if q.dtype != torch.bfloat16:
         raise TypeError("attn_bwd takes bfloat16 q, k, v")
-    for name, t in (("o", o), ("dout", dout)):
-        if t.dtype != torch.bfloat16 or tuple(t.shape) != (B, H, N, d) or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor of shape {(B, H, N, d)}")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
-        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(B, H, N)}")
+    shape = (B, H, N, d)
+    _require("o", o, q.device, torch.bfloat16, shape)
+    _require("dout", dout, q.device, torch.bfloat16, shape)
+    _require("lse", lse, q.device, torch.float32, (B, H, N))
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _require(name, t, q.device, torch.bfloat16, shape)
     nbytes = bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {q.device}")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     lib = load_library()
-    _check(lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-                        workspace.numel() * workspace.element_size(), B, H, N, d, scale, int(bool(causal)),
-                        _stream_handle(stream, q.device)))
+    with torch.cuda.device(q.device):
+        _check(lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), B, H, N, d, scale, int(bool(causal)),
+                            _stream_handle(stream, q.device)))
     return dq, dk, dv
 
 
