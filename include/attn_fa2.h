@@ -161,6 +161,10 @@ int attn_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o,
  *                      and two fp32 per row, each head's rows padded to a
  *                      multiple of 128), overwritten by every call.
  *   d in {64, 128}; B*H <= 65535.  Other arguments and errors as attn_fwd.
+ * The launch order of a causal backward (key tile by key tile across heads, or
+ * head by head) is chosen from the sizes; the environment variable
+ * ATTN_BWD_GRID_ORDER=key or =head, read at each call, forces one.  dk and dv
+ * do not depend on the order; dq only through the order of its fp32 additions.
  */
 int attn_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes_out);
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

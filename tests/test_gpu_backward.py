@@ -91,3 +91,40 @@ def test_backward_non_default_scale(scale, causal):
         err = np.abs(g.float().cpu().double().numpy() - r).max()
         tol = 2e-2 * np.abs(r).max() + 2e-3
         assert err <= tol, f"{name}: {err:.3e} > {tol:.3e}"
+
+
+@pytest.mark.parametrize("order", ["key", "head"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_backward_in_either_grid_order(order, d, monkeypatch):
+    # A causal backward grid runs key-tile-major or head-major, chosen from the
+    # shape; ATTN_BWD_GRID_ORDER forces one.  Both match the oracle.
+    monkeypatch.setenv("ATTN_BWD_GRID_ORDER", order)
+    got, ref = run_case(2, 3, 513, d, True, seed=31 + d)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        err = np.abs(g - r).max()
+        tol = 2e-2 * np.abs(r).max() + 2e-3
+        assert err <= tol, f"{order} {name}: {err:.3e} > {tol:.3e}"
+
+
+def _grads(B, H, N, d, causal, seed):
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed)
+    do = inputs.make_dout_f32(B, H, N, d, seed=seed + 1)
+    dev = [inputs.to_bf16(t).cuda() for t in (q, k, v, do)]
+    o, lse = binding.attn_fwd(dev[0], dev[1], dev[2], causal=causal)
+    grads = binding.attn_bwd(dev[0], dev[1], dev[2], o, lse, dev[3], causal=causal)
+    torch.cuda.synchronize()
+    assert binding.get_device_status() == 0
+    return [g.float().cpu() for g in grads]
+
+
+def test_long_causal_backward_is_the_same_in_both_grid_orders(monkeypatch):
+    # The long causal shape (B=1, H=8, N=32768, d=128), where the shape rule picks
+    # head-major: each CTA computes the dK, dV rows of its own key tile whatever
+    # the order, so they are bit-identical to the key-tile-major run; dQ differs
+    # only by the order of its fp32 reduce-adds.
+    monkeypatch.setenv("ATTN_BWD_GRID_ORDER", "key")
+    a = _grads(1, 8, 32768, 128, True, seed=41)
+    monkeypatch.delenv("ATTN_BWD_GRID_ORDER")
+    b = _grads(1, 8, 32768, 128, True, seed=41)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert float((a[0] - b[0]).abs().max()) <= 1e-3 * max(1.0, float(a[0].abs().max()))

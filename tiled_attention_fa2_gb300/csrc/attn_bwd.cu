@@ -37,6 +37,9 @@
 // them to read the slot before loading the query tile after next into it, so
 // neither the reduce nor its completion sits on the pass warps' path.  After the
 // last query tile: dK * scale and dV to bf16.
+#include <cstdlib>
+#include <cstring>
+
 #include <cuda_bf16.h>
 
 #include "attn_kernels.h"
@@ -333,7 +336,8 @@ __device__ __forceinline__ void tmem_st8x2_issue(uint32_t ta, const uint32_t (&a
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <int D, bool kCausal>
-__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p,
+                                                                      int head_major) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -363,7 +367,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, n_kt = (N + 127) >> 7, n_pad = n_kt * 128;
   const int x = static_cast<int>(blockIdx.x);
-  const int j = kCausal ? x / p.BH : x % n_kt, bh = kCausal ? x % p.BH : x / n_kt;
+  // Grid order: key-tile-major (all heads' key tile 0, then key tile 1, ...: the
+  // heaviest causal CTAs first) or head-major (one head's key tiles after the
+  // other, heaviest first within the head, so the CTAs running together reduce
+  // into one head's dQ, which stays in L2).  Non-causal grids are always
+  // head-major.
+  const bool hm = !kCausal || head_major != 0;
+  const int j = hm ? x % n_kt : x / p.BH, bh = hm ? x / n_kt : x % p.BH;
   const int n_it = kCausal ? n_kt - j : n_kt;  // causal: query tiles j .. n_kt - 1
   // Query tile of this CTA's t-th step.
   auto qtile = [&](int t) { return kCausal || j + t < n_kt ? j + t : j + t - n_kt; };
@@ -632,13 +642,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   }
 }
 
+// Grid order of a causal backward.  Key-tile-major puts the heaviest CTAs
+// (key tile 0 sees every query tile) first across all heads, which balances the
+// SMs best, but the CTAs running together then reduce into every head's dQ at
+// once.  Head-major keeps one head's dQ in L2 at the cost of a coarser balance.
+// It is chosen when the fp32 dQ accumulator exceeds half of L2 and the heaviest
+// CTA (n_kt query tiles) is at most a fifth of an SM's share of the grid's work
+// (BH n_kt (n_kt + 1) / 2 query tiles over the SMs), i.e. 10 SMs <= BH (n_kt + 1).
+// ATTN_BWD_GRID_ORDER=key or =head in the environment overrides the choice.
+cudaError_t causal_head_major(const BwdParams& p, int d, int* out) {
+  const char* env = std::getenv("ATTN_BWD_GRID_ORDER");
+  if (env && std::strcmp(env, "head") == 0) return *out = 1, cudaSuccess;
+  if (env && std::strcmp(env, "key") == 0) return *out = 0, cudaSuccess;
+  int dev = 0, sms = 0, l2 = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
+  const long long n_kt = (p.N + 127) / 128;
+  const long long acc_bytes = static_cast<long long>(p.BH) * p.N * d * 4;
+  *out = (2 * acc_bytes > l2 && 10LL * sms <= static_cast<long long>(p.BH) * (n_kt + 1)) ? 1 : 0;
+  return cudaSuccess;
+}
+
 template <int D, bool kCausal>
 cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   auto kern = attn_bwd_tc_kernel<D, kCausal>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
+  int head_major = 1;
+  if (kCausal && (e = causal_head_major(p, D, &head_major)) != cudaSuccess) return e;
   const long long n_kt = (p.N + 127) / 128;
-  kern<<<static_cast<unsigned>(n_kt * p.BH), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p);
+  kern<<<static_cast<unsigned>(n_kt * p.BH), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p, head_major);
   return cudaGetLastError();
 }
 
