@@ -68,9 +68,9 @@ struct BwdParams {
   const void* o;        // bf16 [BH, N, d] (forward output)
   const void* dout;     // bf16 [BH, N, d] (upstream gradient dO)
   const float* lse;     // fp32 [BH, N], natural log (forward's L)
-  float* lse2;          // fp32 [BH, n_pad] workspace: L * log2 e per row, +inf on padding rows
-  float* drow;          // fp32 [BH, n_pad] workspace: D = rowsum(dO * O), 0 on padding rows
-                        //   (n_pad = N rounded up to a multiple of 128)
+  float* lse2;          // fp32 [BH, n_pad] workspace: -L * log2 e per row, -inf on padding rows
+  float* drow;          // fp32 [BH, n_pad] workspace: -D, D = rowsum(dO * O), 0 on padding rows
+                        //   (n_pad = N rounded up to a multiple of 128; negated so the pass adds them)
   float* dq_acc;        // fp32 [BH, N, d] workspace: dQ accumulator
   void* dq;             // bf16 [BH, N, d]
   void* dk;             // bf16 [BH, N, d]
