@@ -1,0 +1,208 @@
+"""A model of the tensor-core forward kernel's mbarrier protocol (no GPU).
+
+The role loops of attn_fwd_tc_kernel (the TMA producer warp, the MMA warp and
+the eight softmax warps of the two query tiles) are transcribed here at the
+level of their barrier operations. TMA loads land in any order and tcgen05
+commits complete in issue order, at random times. For random interleavings
+over causal and non-causal item lists (ragged N, odd pair counts, one or many
+items per CTA, both ring depths) the model checks two things: no schedule
+deadlocks, and every wait observes exactly the phase it targets. mbarrier
+try_wait.parity compares parities only, so a barrier two phases ahead of its
+waiter (or one behind) would pass or block wrongly on the GPU. The model must
+change together with the kernel's role loops.
+"""
+
+import random
+
+import pytest
+
+
+class Barrier:
+    """An mbarrier: `count` arrivals complete a phase; `done` counts completed phases."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.done = name, count, 0, 0
+
+    def arrive(self):
+        self.pending += 1
+        assert self.pending <= self.count, f"{self.name}: too many arrivals"
+        if self.pending == self.count:
+            self.pending, self.done = 0, self.done + 1
+
+
+def wait_phase(b, phase):
+    """Wait, as try_wait.parity does, for phase `phase` of barrier `b` to complete;
+    fail if the barrier is not exactly at that phase or the one after it."""
+    while (b.done & 1) == (phase & 1):  # the parity test the hardware makes
+        assert b.done == phase, f"{b.name}: waiting for phase {phase} with {b.done} complete"
+        yield "blocked"
+    assert b.done == phase + 1, f"{b.name}: passed phase {phase} with {b.done} complete"
+
+
+def items_of(causal, BH, n_pairs, n_kt, G, cta):
+    """The (key tiles of query tile 0, of query tile 1) of each item CTA `cta` takes (snake order)."""
+    total = BH * n_pairs
+    r = 0
+    while r * G < total:
+        item = r * G + ((G - 1 - cta) if r & 1 else cta)
+        if item < total:
+            if causal:
+                pair = n_pairs - 1 - item // BH
+                yield min(2 * pair + 1, n_kt), min(2 * pair + 2, n_kt)
+            else:
+                yield n_kt, n_kt
+        r += 1
+
+
+def run(seed, causal, BH, N, G, stages):
+    rng = random.Random(seed)
+    n_kt, n_pairs = (N + 127) // 128, (N + 255) // 256
+    G = min(G, BH * n_pairs)  # the persistent grid: at most one CTA per item
+    items = list(items_of(causal, BH, n_pairs, n_kt, G, rng.randrange(G)))
+    assert items
+    bars = {}
+    for t in (0, 1):
+        for name, count in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("p_lo", 4), ("p_hi", 4),
+                            ("o_full", 1), ("o_empty", 4)):
+            bars[f"{name}{t}"] = Barrier(f"{name}{t}", count)
+    for i in range(stages):
+        bars[f"slot_full{i}"] = Barrier(f"slot_full{i}", 1)
+        bars[f"slot_empty{i}"] = Barrier(f"slot_empty{i}", 1)
+    loads = []    # landed in any order
+    commits = []  # completed in issue order
+
+    def wait(name, phase):
+        return wait_phase(bars[name], phase)
+
+    def load(name):
+        loads.append(name)
+
+    def commit(name):
+        commits.append(name)
+
+    def producer():
+        it = nq = 0
+
+        def load_kv():
+            nonlocal it
+            if it >= stages:
+                yield from wait(f"slot_empty{it % stages}", it // stages - 1)
+            load(f"slot_full{it % stages}")
+            it += 1
+
+        def load_q(t):
+            if nq > 0:
+                yield from wait(f"q_empty{t}", nq - 1)
+            load(f"q_full{t}")
+
+        for k0, k1 in items:
+            yield from load_q(0)
+            yield from load_kv()
+            yield from load_q(1)
+            nq += 1
+            for _ in range(1, 2 * k1):
+                yield from load_kv()
+
+    def mma():
+        it = nq = 0
+        npv = [0, 0]
+        for k0, k1 in items:
+            yield from wait("q_full0", nq)
+            yield from wait(f"slot_full{it % stages}", it // stages)
+            commit("s_full0")
+            if k0 == 1:
+                commit("q_empty0")
+            yield from wait("q_full1", nq)
+            commit("s_full1")
+            if k1 == 1:
+                commit("q_empty1")
+            commit(f"slot_empty{it % stages}")
+            it += 1
+            for j in range(k1):
+                sv = it % stages
+                yield from wait(f"slot_full{sv}", it // stages)
+                itk = it + 1
+                k_ready = False
+                for t in (0, 1):
+                    kv_end = k1 if t else k0
+                    if j < kv_end:
+                        if j == 0 and nq > 0:
+                            yield from wait(f"o_empty{t}", nq - 1)
+                        yield from wait(f"p_lo{t}", npv[t])
+                        yield from wait(f"p_hi{t}", npv[t])
+                        npv[t] += 1
+                        if j == kv_end - 1:
+                            commit(f"o_full{t}")
+                    if t == 1:
+                        commit(f"slot_empty{sv}")
+                    if j + 1 < kv_end:
+                        if not k_ready:
+                            yield from wait(f"slot_full{itk % stages}", itk // stages)
+                            k_ready = True
+                        commit(f"s_full{t}")
+                        if j + 2 == kv_end:
+                            commit(f"q_empty{t}")
+                if j + 1 < k1:
+                    commit(f"slot_empty{itk % stages}")
+                it += 2 if j + 1 < k1 else 1
+            nq += 1
+
+    def softmax_warp(t):
+        ns = nq = 0
+        for k0, k1 in items:
+            for _ in range(k1 if t else k0):
+                yield from wait(f"s_full{t}", ns)
+                ns += 1
+                yield "work"
+                bars[f"p_lo{t}"].arrive()
+                yield "work"
+                bars[f"p_hi{t}"].arrive()
+            yield from wait(f"o_full{t}", nq)
+            bars[f"o_empty{t}"].arrive()
+            nq += 1
+
+    roles = [producer(), mma()] + [softmax_warp(t) for t in (0, 1) for _ in range(4)]
+    alive = list(range(len(roles)))
+    idle = 0
+    while alive:
+        if loads and rng.random() < 0.3:
+            bars[loads.pop(rng.randrange(len(loads)))].arrive()
+            idle = 0
+        if commits and rng.random() < 0.3:
+            bars[commits.pop(0)].arrive()
+            idle = 0
+        r = rng.choice(alive)
+        try:
+            step = next(roles[r])
+        except StopIteration:
+            alive.remove(r)
+            idle = 0
+            continue
+        idle = idle + 1 if step == "blocked" else 0
+        assert not (idle > 200 * len(alive) and not loads and not commits), f"deadlock, roles {alive} waiting"
+    return True
+
+
+CASES = [(True, 64, 2048, 152, 5), (True, 3, 300, 4, 5), (False, 2, 1000, 3, 8), (True, 1, 37, 1, 8),
+         (False, 1, 1892, 2, 8), (True, 2, 640, 2, 5)]
+
+
+@pytest.mark.parametrize("causal,BH,N,G,stages", CASES)
+def test_forward_barrier_protocol_has_no_deadlock_or_phase_aliasing(causal, BH, N, G, stages):
+    for seed in range(12):
+        assert run(seed, causal, BH, N, G, stages)
+
+
+def test_the_model_catches_a_barrier_two_phases_ahead():
+    # Two completed phases look like none to a parity test: the model must report
+    # the waiter that missed one, not let it block (or pass) silently.
+    b = Barrier("x", 1)
+    b.arrive()
+    b.arrive()
+    with pytest.raises(AssertionError):
+        next(wait_phase(b, 0))
+    # one phase ahead is the normal case: the waiter passes
+    c = Barrier("y", 1)
+    c.arrive()
+    with pytest.raises(StopIteration):
+        next(wait_phase(c, 0))
