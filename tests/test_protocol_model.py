@@ -206,3 +206,111 @@ def test_the_model_catches_a_barrier_two_phases_ahead():
     c.arrive()
     with pytest.raises(StopIteration):
         next(wait_phase(c, 0))
+
+
+def run_backward(seed, n_it, slots, double_s):
+    """The backward kernel's CTA (one key tile, n_it query tiles): producer, MMA
+    warp and the eight pass warps, with `slots` Q/dO slots and, when
+    `double_s`, the next query tile's S^T issued into a second buffer during
+    the current pass (the d = 64 layout)."""
+    rng = random.Random(seed)
+    bars = {name: Barrier(name, count) for name, count in (
+        ("kv", 1), ("s_full", 1), ("dq_full", 1), ("drain_done", 8), ("fin", 1), ("p_full0", 8), ("p_full1", 8))}
+    for s in range(slots):
+        for name, count in (("q_full", 1), ("q_empty", 1), ("stage_free", 8)):
+            bars[f"{name}{s}"] = Barrier(f"{name}{s}", count)
+    loads, commits = [], []
+
+    def slot(t):
+        return t % slots
+
+    def use(t):
+        return t // slots  # phase index of slot(t)'s barriers for query tile t
+
+    def wait(name, phase):
+        return wait_phase(bars[name], phase)
+
+    reduced = []
+
+    def producer():
+        loads.append("kv")
+
+        def finish_tile(t):  # dQ of tile t staged: reduce-add it, then the slot is free
+            yield from wait(f"stage_free{slot(t)}", use(t))
+            reduced.append(t)
+            yield "work"
+
+        for it in range(n_it):
+            if it >= slots:
+                yield from finish_tile(it - slots)
+            loads.append(f"q_full{slot(it)}")
+        for t in range(max(0, n_it - slots), n_it):
+            yield from finish_tile(t)
+
+    def mma():
+        yield from wait("kv", 0)
+        yield from wait("q_full0", 0)
+        commits.append("s_full")
+        for it in range(n_it):
+            s = slot(it)
+            if double_s and it + 1 < n_it:
+                yield from wait(f"q_full{slot(it + 1)}", use(it + 1))
+                if it > 0:
+                    yield from wait("drain_done", it - 1)
+            yield from wait("p_full0", it)
+            yield from wait("p_full1", it)
+            commits.append(f"q_empty{s}")
+            commits.append("dq_full")
+            if it + 1 < n_it:
+                if not double_s:
+                    yield from wait(f"q_full{slot(it + 1)}", use(it + 1))
+                    yield from wait("drain_done", it)
+                commits.append("s_full")
+        commits.append("fin")
+        yield from wait("fin", 0)
+
+    def pass_warp():
+        for it in range(n_it):
+            s = slot(it)
+            yield from wait("s_full", it)
+            yield from wait(f"q_full{s}", use(it))
+            yield "work"
+            bars["p_full0"].arrive()
+            yield "work"
+            bars["p_full1"].arrive()
+            yield from wait("dq_full", it)
+            yield "work"
+            bars["drain_done"].arrive()
+            yield from wait(f"q_empty{s}", use(it))
+            yield "work"
+            bars[f"stage_free{s}"].arrive()
+        yield from wait("fin", 0)
+
+    roles = [producer(), mma()] + [pass_warp() for _ in range(8)]
+    alive = list(range(len(roles)))
+    idle = 0
+    while alive:
+        if loads and rng.random() < 0.3:
+            bars[loads.pop(rng.randrange(len(loads)))].arrive()
+            idle = 0
+        if commits and rng.random() < 0.3:
+            bars[commits.pop(0)].arrive()
+            idle = 0
+        r = rng.choice(alive)
+        try:
+            step = next(roles[r])
+        except StopIteration:
+            alive.remove(r)
+            idle = 0
+            continue
+        idle = idle + 1 if step == "blocked" else 0
+        assert not (idle > 200 * len(alive) and not loads and not commits), f"deadlock, roles {alive} waiting"
+    assert sorted(reduced) == list(range(n_it)), "every query tile's dQ is reduced exactly once"
+    return True
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("slots,double_s", [(2, False), (3, True)])
+def test_backward_barrier_protocol_has_no_deadlock_or_phase_aliasing(n_it, slots, double_s):
+    for seed in range(12):
+        assert run_backward(seed, n_it, slots, double_s)
