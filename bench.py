@@ -595,6 +595,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} needs one process per GPU (torchrun --nproc-per-node {args.gpus}); "
+                 f"this launch has WORLD_SIZE={world}")
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference_arm(args, w)

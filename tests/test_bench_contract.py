@@ -83,3 +83,16 @@ def test_committed_traffic_records_are_well_formed():
 @pytest.mark.parametrize("world,steps,ms,expect", [(1, 10, 20.0, 1000.0), (4, 10, 20.0, 4000.0)])
 def test_job_throughput_counts_every_rank(world, steps, ms, expect):
     assert bench.job_throughput(2e12, world, steps, ms) == pytest.approx(expect)
+
+
+def test_gpu_count_must_match_the_launch():
+    # --gpus N is one process per GPU under torchrun; a single process asking for
+    # two GPUs is refused instead of silently timing one.
+    import subprocess
+    import sys
+
+    env = dict(os.environ)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"), "--gpus", "2",
+                        "--impl", "reference"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 2 and "WORLD_SIZE=1" in r.stderr
