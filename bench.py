@@ -2,8 +2,10 @@
 """Throughput of the attention forward on GB300: one JSON line.
 
 A step is one attention forward (every step of the fused path, in one kernel)
-over one batch of the workload.  Default workload: bf16 causal LM prefill,
-B=4, H=16, N=2048, d=128.  Inputs are resident in HBM before timing; L2 is
+over one batch of the workload.  Default workload: the FP8 DiT-block attention
+shaped like the one the FP8 CuTe-DSL page times (B=1, H=56, N=30272, d=128,
+e4m3 Q/K/V with per-tensor descales, non-causal), the largest single-GPU
+workload.  Inputs are resident in HBM before timing; L2 is
 flushed (a 512 MiB device write) before every timed step, outside the timed
 interval; each step is timed with CUDA events on the stream the kernel runs
 on, and the sum over the K steps gives the throughput.
@@ -40,7 +42,7 @@ from tiled_attention_fa2_gb300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOPS & % of GB300 dense bf16/fp8 tensor peak; ms per call"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "prefill_causal_bf16"
+DEFAULT_WORKLOAD = "dit_e4m3"
 FLUSH_BYTES = 512 << 20
 # Published figures for an exact workload (other hardware: context only).
 PUBLISHED_TFLOPS = {"dit_e4m3": 26.27e12 / 123.6e-3 / 1e12}  # RTX 5080, final FP8 CuTe-DSL kernel
@@ -98,16 +100,18 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 20):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -115,7 +119,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The host-time interval of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -128,7 +136,10 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # Only samples printed while the timed region ran count (nvidia-smi prints a
+        # sample when it has taken it, so the host time of the line bounds it).
+        lines = [ln for t, ln in self.lines if self.window is None or self.window[0] <= t <= self.window[1]]
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -141,7 +152,8 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples_under_load": len(sm),
+                "interval_ms": self.interval_ms}
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:
@@ -161,9 +173,14 @@ def job_throughput(flops_per_step: float, world: int, steps: int, max_ms: float)
     return flops_per_step * world * steps / (max_ms * 1e-3) / 1e12
 
 
+def kv_heads(w: dict) -> int:
+    """K/V heads of a workload (fewer than H under grouped-query attention)."""
+    return int(w.get("Hkv", w["H"]))
+
+
 def make_device_inputs(w: dict, device, seed: int):
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
-    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=w["q_mult"])
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=w["q_mult"], n_kv_heads=kv_heads(w))
     descales = (1.0, 1.0, 1.0)
     if w["dtype"] == "bf16":
         host = tuple(inputs.to_bf16(t) for t in (q, k, v))
@@ -203,8 +220,13 @@ def run_gpu_arm(args, w):
     sh = stream.cuda_stream
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
+    Hkv = kv_heads(w)
+
     def launch():
-        if code == 2:
+        if Hkv != H:
+            st = lib.attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv,
+                                  N, d, scale, *descales, int(causal), code, sh)
+        elif code == 2:
             st = lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
                                   scale, *descales, int(causal), sh)
         else:
@@ -232,9 +254,11 @@ def run_gpu_arm(args, w):
         launch()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    t1 = time.perf_counter()
     if dist:
         dist.barrier()
     wall = time.perf_counter() - t0
+    sampler.mark(t0, t1)
     clocks = sampler.stop()
     st = binding.get_device_status()
     if st != 0:
@@ -264,6 +288,20 @@ def run_gpu_arm(args, w):
     def e2e_call(i):
         st_obj, bufs = e2e_streams[i % 2], e2e_sets[i % 2]
         d_in = bufs["d_in"]
+        if Hkv != H:
+            # Grouped-query attention has no host entry point: the same copies
+            # through the stream, then attn_fwd_gqa, then the copies back.
+            with torch.cuda.stream(st_obj):
+                for dst, src in zip(d_in, h_in):
+                    dst.copy_(src, non_blocking=True)
+                st = lib.attn_fwd_gqa(d_in[0].data_ptr(), d_in[1].data_ptr(), d_in[2].data_ptr(),
+                                      bufs["o"].data_ptr(), bufs["lse"].data_ptr(), B, H, Hkv, N, d, scale,
+                                      *descales, int(causal), code, st_obj.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(lib.attn_last_error().decode())
+                bufs["h_o"].copy_(bufs["o"], non_blocking=True)
+                bufs["h_l"].copy_(bufs["lse"], non_blocking=True)
+            return
         st = lib.attn_fwd_host(h_in[0].data_ptr(), h_in[1].data_ptr(), h_in[2].data_ptr(), bufs["h_o"].data_ptr(),
                                bufs["h_l"].data_ptr(), d_in[0].data_ptr(), d_in[1].data_ptr(), d_in[2].data_ptr(),
                                bufs["o"].data_ptr(), bufs["lse"].data_ptr(), B, H, N, d, scale, *descales,
@@ -309,7 +347,7 @@ def run_gpu_arm(args, w):
         "vs_baseline": round(value / PUBLISHED_TFLOPS[args.workload], 3) if args.workload in PUBLISHED_TFLOPS else None,
         "dtype": w["dtype"],
         "data": "synthetic: i.i.d. N(0,1) Q/K/V from a seeded CPU generator (seed = rank)",
-        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": bool(causal),
+        "config": {"workload": args.workload, "B": B, "H": H, "H_kv": Hkv, "N": N, "d": d, "causal": bool(causal),
                    "flops_per_step": flops, "l2": "flushed before every timed step (512 MiB device write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": round(100.0 * achieved / peak, 2),
@@ -333,18 +371,22 @@ def run_gpu_arm(args, w):
 
 
 def _oracle_head_inputs(w, host, descales, h):
+    """Query head h (over B*H) and the K/V head it reads, decoded by the oracle."""
     import oracle
 
     fmt = w["dtype"]
-    BHN = (w["B"] * w["H"], w["N"], w["d"])
+    H, Hkv = w["H"], kv_heads(w)
+    b, hq = divmod(h, H)
+    hk = b * Hkv + oracle.kv_head_of(hq, H, Hkv)
     out = []
-    for t, ds in zip(host, descales):
+    for t, ds, i in zip(host, descales, (h, hk, hk)):
+        shape = (-1, w["N"], w["d"])
         if fmt == "bf16":
-            c = inputs.bits_u16(t).reshape(BHN)[h]
+            c = inputs.bits_u16(t).reshape(shape)[i]
         elif fmt == "e4m3":
-            c = inputs.bits_u8(t).reshape(BHN)[h]
+            c = inputs.bits_u8(t).reshape(shape)[i]
         else:
-            c = t.reshape(BHN)[h].numpy()
+            c = t.reshape(shape)[i].numpy()
         out.append(oracle.dequantize(c, fmt, ds))
     return out
 
@@ -437,8 +479,8 @@ def run_reference_arm(args, w):
     line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same recipe as the GPU arm)",
-            "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
-                       "causal": bool(w["causal"])},
+            "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "H_kv": kv_heads(w), "N": w["N"],
+                       "d": w["d"], "causal": bool(w["causal"])},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(), "cpu": cpu_model(),
                              "kind": "oracle", "sample": sample},
@@ -448,7 +490,8 @@ def run_reference_arm(args, w):
 
 
 def make_host_inputs(w):
-    q, k, v = inputs.make_qkv_f32(w["B"], w["H"], w["N"], w["d"], seed=0, q_mult=w["q_mult"])
+    q, k, v = inputs.make_qkv_f32(w["B"], w["H"], w["N"], w["d"], seed=0, q_mult=w["q_mult"],
+                                  n_kv_heads=kv_heads(w))
     if w["dtype"] == "bf16":
         return tuple(inputs.to_bf16(t) for t in (q, k, v)), (1.0, 1.0, 1.0)
     if w["dtype"] == "e4m3":
@@ -508,6 +551,7 @@ def run_gpu_bwd(args, w):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    sampler.mark(t0, t0 + wall)
     clocks = sampler.stop()
     if binding.get_device_status() != 0:
         raise RuntimeError("device status set after the timed region")
@@ -603,6 +647,8 @@ def main():
     if args.impl == "reference":
         run_reference_arm(args, w)
     elif args.pass_ == "bwd":
+        if kv_heads(w) != w["H"]:
+            ap.error("the backward is implemented for multi-head attention only (H_kv = H)")
         run_gpu_bwd(args, w)
     else:
         run_gpu_arm(args, w)

@@ -80,6 +80,25 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, float q_descale, float k_descale, float v_descale, int causal, void* stream);
 
 /*
+ * Grouped-query attention forward ("Kernels and Memory in LLM Inference",
+ * "Store less: MQA, GQA, MLA", "Grouped-query attention (2023)": the query
+ * heads are split into groups, and each group reads one K/V head of its own;
+ * H_kv = 1 is multi-query attention, H_kv = H ordinary multi-head attention).
+ *   q, o, lse : as attn_fwd, with H query heads.
+ *   k, v      : device, [B, H_kv, N, d] of `dtype`.
+ *   H_kv      : number of K/V heads, >= 1, dividing H.  Query head h reads K/V
+ *               head h / (H / H_kv): a group is H / H_kv consecutive query
+ *               heads (the pages do not say which heads form a group).
+ *   descales  : used for ATTN_E4M3 only (as attn_fwd_fp8), ignored otherwise.
+ * Same kernels, dtypes, head dimensions and causal modes as attn_fwd; the
+ * shared K/V tiles are fetched once per group from L2.  Invalid H / H_kv:
+ * ATTN_ERR_INVALID_ARG, nothing launched.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d, float scale, float q_descale, float k_descale, float v_descale, int causal, int dtype,
+                 void* stream);
+
+/*
  * End-to-end forward from host buffers, for callers whose data lives in host
  * memory: enqueues on `stream` the copies h_q/h_k/h_v -> d_q/d_k/d_v, the
  * forward (as attn_fwd_fp8 for ATTN_E4M3, attn_fwd otherwise; descales are
@@ -132,10 +151,15 @@ int attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* 
  * allocates nothing.
  *   - Sizes whose planned workspace (attn_fwd_split_plan) exceeds 64 MiB are
  *     rejected with ATTN_ERR_UNSUPPORTED; other arguments as attn_fwd_split.
- *   - Every GPU that loads the library keeps the 64 MiB array until exit.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *   - The array belongs to the library's device code, which CUDA loads onto a
+ *     device lazily (by default): the first call on a device loads it there,
+ *     which commits the 64 MiB, and looks up the array's device address (once
+ *     per device, with that device current).  That first call can therefore
+ *     fail with ATTN_ERR_CUDA (out of memory) where later calls cannot; make it
+ *     at set-up time, before any stream capture.  From then on the device keeps
+ *     the array until the process exits.
+ *   - The looked-up address is cached per device ordinal: do not call
+ *     cudaDeviceReset on a device while this library is in use there.
  *   - All calls share the array, which keeps the last call's contents; every
  *     byte a call reads it has written first, so nothing needs clearing.
  *     Calls whose work overlaps on the GPU (several streams or threads) race on

@@ -18,6 +18,9 @@ Sources the oracle follows (page title, then the section or listing cited):
 * "1.8x Faster Attention on an RTX 5080: an FP8 Flash Attention Kernel in
   CuTe-DSL", sections "The attention itself" (online softmax worked example) and
   "Who am I, what's mine?" (FP8 descales folded into the score scale).
+* Grouped-query attention ("Kernels and Memory in LLM Inference", "Store less:
+  MQA, GQA, MLA", "Grouped-query attention (2023)"): groups of query heads share
+  one K/V head; each query head is ordinary attention against its group's head.
 * The backward pass ("FlashAttention-2 from PyTorch to Triton", item 5 of the
   list of what its first kernel leaves out; "Kernels and Memory in LLM
   Inference", "Training detour (brief)"): P rebuilt from L, D = rowsum(dO * O),
@@ -37,6 +40,9 @@ from .attention import (  # noqa: F401
     attention_reference,
     attention_rows,
     attention_tiled,
+    kv_head_of,
+    attention_gqa,
+    attention_gqa_rows,
     attention_backward,
     attention_backward_tiled,
 )

@@ -182,6 +182,74 @@ def attention_rows(q, k, v, rows, scale: float, causal: bool = False):
 
 
 # --------------------------------------------------------------------------
+# Grouped-query attention: query heads share K/V heads.
+# --------------------------------------------------------------------------
+
+
+def kv_head_of(h: int, n_heads: int, n_kv_heads: int) -> int:
+    """The K/V head that query head ``h`` reads under grouped-query attention.
+
+    "Kernels and Memory in LLM Inference", "Store less: MQA, GQA, MLA",
+    "Grouped-query attention (2023)": the query heads are split into groups
+    and each group gets one K/V head of its own; one group is multi-query
+    attention, one group per head is ordinary multi-head attention.  The page
+    does not say which query heads form a group; here a group is
+    ``n_heads // n_kv_heads`` consecutive query heads, so group ``g`` (query
+    heads ``g*G .. g*G + G - 1``) reads K/V head ``g``.
+    """
+    if n_kv_heads < 1 or n_heads % n_kv_heads != 0:
+        raise ValueError(f"n_heads ({n_heads}) must be a multiple of n_kv_heads ({n_kv_heads})")
+    if not 0 <= h < n_heads:
+        raise ValueError(f"head {h} out of range")
+    return h // (n_heads // n_kv_heads)
+
+
+def attention_gqa(q, k, v, scale: float, causal: bool = False):
+    """Grouped-query attention forward in float64.
+
+    ``q``: [B, H, N, d]; ``k``, ``v``: [B, H_kv, N, d] with H a multiple of
+    H_kv.  Query head h of batch b is ordinary attention
+    (:func:`attention_reference`) against K/V head ``kv_head_of(h, H, H_kv)``
+    of batch b.  Returns O [B, H, N, d] and L [B, H, N].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, n, _ = q.shape
+    hkv = k.shape[1]
+    o = np.empty(q.shape[:3] + (v.shape[-1],))
+    lse = np.empty((B, H, n))
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, hkv)
+            o[b, h], lse[b, h] = attention_reference(q[b, h], k[b, g], v[b, g], scale, causal)
+    return o, lse
+
+
+def attention_gqa_rows(q, k, v, rows, scale: float, causal: bool = False):
+    """Selected query rows of :func:`attention_gqa`.
+
+    ``q``: [B, H, N, d]; ``k``, ``v``: [B, H_kv, N, d]; ``rows``: int array
+    [B*H, R] (rows of query head (b, h) are ``rows[b*H + h]``).  Returns
+    O [B*H, R, d] and L [B*H, R].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    B, H = q.shape[:2]
+    hkv = k.shape[1]
+    o = np.empty((B * H, rows.shape[1], v.shape[-1]))
+    lse = np.empty((B * H, rows.shape[1]))
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, hkv)
+            r = rows[b * H + h]
+            o[b * H + h], lse[b * H + h] = _attention_one_head(q[b, h][r], r, k[b, g], v[b, g], scale, causal)
+    return o, lse
+
+
+# --------------------------------------------------------------------------
 # Tile-by-tile online-softmax re-derivation (tiny inputs only).
 # --------------------------------------------------------------------------
 

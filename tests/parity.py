@@ -34,36 +34,43 @@ class Case:
     codes: tuple                # numpy arrays handed to the oracle ([BH, N, d] each)
     descales: tuple = (1.0, 1.0, 1.0)
     scale_override: float | None = None  # softmax scale other than 1/sqrt(d)
+    Hkv: int | None = None      # K/V heads (grouped-query attention); None = H
 
     @property
     def scale(self):
         return self.scale_override if self.scale_override is not None else 1.0 / math.sqrt(self.d)
 
 
-def make_case(B, H, N, d, dtype, seed=0, q_mult=1.0) -> Case:
-    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=q_mult)
+def make_case(B, H, N, d, dtype, seed=0, q_mult=1.0, n_kv_heads=None) -> Case:
+    """Seeded inputs; ``codes`` are [heads, N, d] per tensor (K and V have
+    B * n_kv_heads heads under grouped-query attention)."""
+    q, k, v = inputs.make_qkv_f32(B, H, N, d, seed=seed, q_mult=q_mult, n_kv_heads=n_kv_heads)
+    hkv = None if n_kv_heads is None or n_kv_heads == H else int(n_kv_heads)
+    shape = (-1, N, d)
     if dtype == "f32":
         stored = (q, k, v)
-        codes = tuple(t.reshape(B * H, N, d).numpy() for t in stored)
-        return Case(B, H, N, d, dtype, stored, codes)
+        codes = tuple(t.reshape(shape).numpy() for t in stored)
+        return Case(B, H, N, d, dtype, stored, codes, Hkv=hkv)
     if dtype == "bf16":
         stored = tuple(inputs.to_bf16(t) for t in (q, k, v))
-        codes = tuple(inputs.bits_u16(t).reshape(B * H, N, d) for t in stored)
-        return Case(B, H, N, d, dtype, stored, codes)
+        codes = tuple(inputs.bits_u16(t).reshape(shape) for t in stored)
+        return Case(B, H, N, d, dtype, stored, codes, Hkv=hkv)
     if dtype == "e4m3":
         qc, qd = inputs.quantize_e4m3(q)
         kc, kd = inputs.quantize_e4m3(k)
         vc, vd = inputs.quantize_e4m3(v)
         stored = (qc, kc, vc)
-        codes = tuple(inputs.bits_u8(t).reshape(B * H, N, d) for t in stored)
-        return Case(B, H, N, d, dtype, stored, codes, (qd, kd, vd))
+        codes = tuple(inputs.bits_u8(t).reshape(shape) for t in stored)
+        return Case(B, H, N, d, dtype, stored, codes, (qd, kd, vd), Hkv=hkv)
     raise ValueError(dtype)
 
 
 def run_gpu(case: Case, causal: bool):
     """One forward through the C ABI; returns (O float64 [BH,N,d], L float64 [BH,N])."""
     dev = [t.cuda() for t in case.stored]
-    if case.dtype == "e4m3":
+    if case.Hkv is not None:
+        o, lse = binding.attn_fwd_gqa(*dev, descales=case.descales, scale=case.scale, causal=causal)
+    elif case.dtype == "e4m3":
         o, lse = binding.attn_fwd_fp8(*dev, *case.descales, scale=case.scale, causal=causal)
     else:
         o, lse = binding.attn_fwd(*dev, scale=case.scale, causal=causal)
@@ -76,8 +83,13 @@ def run_gpu(case: Case, causal: bool):
 
 
 def _head(case: Case, h: int):
+    """Query head h (over B*H) and the K/V head it reads, decoded by the oracle."""
     fmt = case.dtype
-    return tuple(oracle.dequantize(c[h], fmt, ds) for c, ds in zip(case.codes, case.descales))
+    hk = h
+    if case.Hkv is not None:
+        b, hq = divmod(h, case.H)
+        hk = b * case.Hkv + oracle.kv_head_of(hq, case.H, case.Hkv)
+    return tuple(oracle.dequantize(c[i], fmt, ds) for c, ds, i in zip(case.codes, case.descales, (h, hk, hk)))
 
 
 def oracle_full(case: Case, causal: bool):

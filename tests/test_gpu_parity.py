@@ -163,15 +163,10 @@ def test_non_default_scale(dtype, d, scale, causal):
     """The scale multiplies the scores before the softmax (1.5 on unit-variance
     inputs spreads a row over about 30 doublings, so the reference max moves).
 
-    e4m3: a large scale makes rows peaked, and the dominant weight of a row is
-    stored in P as e4m3 (3 mantissa bits, round to nearest: relative error up to
-    2^-4) while l sums it unrounded, so O may be off by up to 2^-4 * max|V| on
-    such rows; that bound (or the 6e-2 bar, whichever is larger) applies here."""
+    e4m3: a large scale makes rows peaked.  P goes through e4m3 (3 mantissa
+    bits), and the kernel divides O by the sum of exactly those rounded weights,
+    so a row's dominant weight carries no rounding error into O and the stated
+    6e-2 bar holds here too; L comes from the unrounded sum (1e-3)."""
     case = make_case(1, 2, 300, d, dtype, seed=int(scale * 100) + d)
     case.scale_override = scale
-    tol_o = None
-    if dtype == "e4m3":
-        vmax = max(float(np.abs(oracle.dequantize(case.codes[2][h], "e4m3", case.descales[2])).max())
-                   for h in range(case.B * case.H))
-        tol_o = max(TOL_O["e4m3"], vmax / 16)
-    _check(case, causal, tight=TOL_F32_TIGHT if dtype == "f32" else None, tol_o=tol_o)
+    _check(case, causal, tight=TOL_F32_TIGHT if dtype == "f32" else None)

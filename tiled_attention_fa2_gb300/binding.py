@@ -26,6 +26,7 @@ _VP, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint
 SIGNATURES = {
     "attn_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP]),
     "attn_fwd_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _VP]),
+    "attn_fwd_gqa": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _VP]),
     "attn_fwd_host": (_I, [_VP] * 10 + [_I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _VP]),
     "attn_get_device_status": (_I, [_VP]),
     "attn_set_wait_limit_ns": (_U64, [_U64]),
@@ -151,6 +152,35 @@ def attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, sca
     with torch.cuda.device(q.device):
         _check(lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,
                                 d, scale, float(q_descale), float(k_descale), float(v_descale), int(bool(causal)),
+                                _stream_handle(stream, q.device)))
+    return o, lse
+
+
+def attn_fwd_gqa(q, k, v, descales=None, o=None, lse=None, scale=None, causal=False, stream=None):
+    """Grouped-query attention forward: q [B, H, N, d]; k, v [B, H_kv, N, d]
+    with H a multiple of H_kv (query head h reads K/V head h // (H // H_kv)).
+    float32, bfloat16, or e4m3 codes with ``descales`` = (q, k, v) descales.
+    Returns (o [B, H, N, d], lse [B, H, N])."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError(f"q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape (got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)})")
+    B, H, N, d = (int(x) for x in q.shape)
+    Hkv = int(k.shape[1])
+    if (int(k.shape[0]), int(k.shape[2]), int(k.shape[3])) != (B, N, d):
+        raise ValueError(f"k, v must be [{B}, H_kv, {N}, {d}] (got {tuple(k.shape)})")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must have the same dtype")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.device != q.device:
+            raise ValueError("q, k, v must be contiguous CUDA tensors on one device")
+    code = _dtype_code(q)
+    o, lse = _outputs(q, o, lse, B, H, N, d, code)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ds = tuple(float(x) for x in descales) if descales is not None else (1.0, 1.0, 1.0)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hkv,
+                                N, d, scale, ds[0], ds[1], ds[2], int(bool(causal)), code,
                                 _stream_handle(stream, q.device)))
     return o, lse
 

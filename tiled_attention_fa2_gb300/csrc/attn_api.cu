@@ -91,9 +91,42 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Recently encoded tensor maps of this thread.  A map is a pure function of
+// its arguments (address, element type, sizes), so an entry stays valid for
+// as long as it is in the table, whatever happened to the memory meanwhile.
+struct MapCacheEntry {
+  const void* base;
+  CUtensorMapDataType dt;
+  int elem_bytes, BH, N, d;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSize = 8;
+thread_local MapCacheEntry g_map_cache[kMapCacheSize];
+thread_local int g_map_cache_used = 0, g_map_cache_next = 0;
+
+int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d);
+
 // 3-D map over a [BH, N, d] tensor: dims (d, N, BH), 128-row boxes of one
 // 128-byte column block, 128-byte swizzle, zero fill outside [0, N).
+// Encoded once per distinct argument set (per thread), then reused.
 int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d) {
+  for (int i = 0; i < g_map_cache_used; ++i) {
+    const MapCacheEntry& e = g_map_cache[i];
+    if (e.base == base && e.dt == dt && e.elem_bytes == elem_bytes && e.BH == BH && e.N == N && e.d == d) {
+      *map = e.map;
+      return ATTN_OK;
+    }
+  }
+  const int st = encode_map(map, base, dt, elem_bytes, BH, N, d);
+  if (st != ATTN_OK) return st;
+  MapCacheEntry& e = g_map_cache[g_map_cache_next];
+  e = MapCacheEntry{base, dt, elem_bytes, BH, N, d, *map};
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
+  if (g_map_cache_used < kMapCacheSize) ++g_map_cache_used;
+  return ATTN_OK;
+}
+
+int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d) {
   auto fn = encode_fn();
   if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -161,7 +194,8 @@ int plan_split(int B, int H, int N, int d, int req, SplitPlan* out) {
 
 int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, float qds, float kds, float vds, int causal, bool fp8, cudaStream_t stream,
-           int n_splits = 1, int kt_per = 0, float* part_o = nullptr, float* part_l = nullptr) {
+           int n_splits = 1, int kt_per = 0, float* part_o = nullptr, float* part_l = nullptr, int Hkv = 0) {
+  if (Hkv == 0) Hkv = H;
   if (fp8 ? (d != 128) : (d != 64 && d != 128))
     return fail(ATTN_ERR_UNSUPPORTED, "%s tensor-core path supports d in %s (got %d)", fp8 ? "e4m3" : "bf16",
                 fp8 ? "{128}" : "{64, 128}", d);
@@ -175,12 +209,14 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
   const int eb = fp8 ? 1 : 2;
   int st;
   if ((st = make_map(&p.tm_q, q, dt, eb, BH, N, d)) != ATTN_OK) return st;
-  if ((st = make_map(&p.tm_k, k, dt, eb, BH, N, d)) != ATTN_OK) return st;
-  if ((st = make_map(&p.tm_v, v, dt, eb, BH, N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_k, k, dt, eb, B * Hkv, N, d)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, dt, eb, B * Hkv, N, d)) != ATTN_OK) return st;
   if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
   p.o = o;
   p.lse = lse;
   p.BH = BH;
+  p.H = H;
+  p.kv_group = H / Hkv;
   p.N = N;
   p.n_pairs = static_cast<int>(n_pairs);
   p.scale_log2 = scale * kLog2e * qds * kds;
@@ -200,7 +236,8 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 int run_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-            float scale, int causal, cudaStream_t stream) {
+            float scale, int causal, cudaStream_t stream, int Hkv = 0) {
+  if (Hkv == 0) Hkv = H;
   if (d != 16 && d != 32 && d != 64 && d != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "fp32 path supports d in {16, 32, 64, 128} (got %d)", d);
   attn::SimtParams p;
@@ -210,6 +247,8 @@ int run_f32(const void* q, const void* k, const void* v, void* o, float* lse, in
   p.o = static_cast<float*>(o);
   p.lse = lse;
   p.BH = B * H;
+  p.H = H;
+  p.kv_group = H / Hkv;
   p.N = N;
   p.scale_log2 = scale * kLog2e;
   cudaError_t e = attn::launch_simt_f32(p, d, causal != 0, stream);
@@ -242,14 +281,19 @@ int check_kernel(const void* o, int B, int H, int N, int d, int dtype) {
 }
 
 int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-             float scale, float qds, float kds, float vds, int causal, int dtype, cudaStream_t stream) {
+             float scale, float qds, float kds, float vds, int causal, int dtype, cudaStream_t stream,
+             int Hkv = 0) {
   int st = check_common(q, k, v, o, lse, B, H, N, d, scale, causal);
   if (st != ATTN_OK) return st;
   if ((st = check_kernel(o, B, H, N, d, dtype)) != ATTN_OK) return st;
   switch (dtype) {
-    case ATTN_F32: return run_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream);
-    case ATTN_BF16: return run_tc(q, k, v, o, lse, B, H, N, d, scale, 1.f, 1.f, 1.f, causal, false, stream);
-    case ATTN_E4M3: return run_tc(q, k, v, o, lse, B, H, N, d, scale, qds, kds, vds, causal, true, stream);
+    case ATTN_F32: return run_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream, Hkv);
+    case ATTN_BF16:
+      return run_tc(q, k, v, o, lse, B, H, N, d, scale, 1.f, 1.f, 1.f, causal, false, stream, 1, 0, nullptr,
+                    nullptr, Hkv);
+    case ATTN_E4M3:
+      return run_tc(q, k, v, o, lse, B, H, N, d, scale, qds, kds, vds, causal, true, stream, 1, 0, nullptr,
+                    nullptr, Hkv);
     default: return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
   }
 }
@@ -292,6 +336,19 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
     return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
   return dispatch(q, k, v, o, lse, B, H, N, d, scale, q_descale, k_descale, v_descale, causal, ATTN_E4M3,
                   static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d, float scale, float q_descale, float k_descale, float v_descale, int causal, int dtype,
+                 void* stream) {
+  g_last_error[0] = '\0';
+  if (H_kv < 1 || H < 1 || H % H_kv != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "H (%d) must be a positive multiple of H_kv (%d)", H, H_kv);
+  const bool fp8 = dtype == ATTN_E4M3;
+  if (fp8 && (!good_descale(q_descale) || !good_descale(k_descale) || !good_descale(v_descale)))
+    return fail(ATTN_ERR_INVALID_ARG, "descales must be finite and > 0");
+  return dispatch(q, k, v, o, lse, B, H, N, d, scale, fp8 ? q_descale : 1.f, fp8 ? k_descale : 1.f,
+                  fp8 ? v_descale : 1.f, causal, dtype, static_cast<cudaStream_t>(stream), H_kv);
 }
 
 int attn_fwd_host(const void* h_q, const void* h_k, const void* h_v, void* h_o, float* h_lse, void* d_q,

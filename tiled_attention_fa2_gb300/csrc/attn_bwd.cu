@@ -668,7 +668,8 @@ cudaError_t causal_head_major(const BwdParams& p, int d, int* out) {
 template <int D, bool kCausal>
 cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   auto kern = attn_bwd_tc_kernel<D, kCausal>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
+  static std::atomic<unsigned long long> opted_in{0};
+  cudaError_t e = smem_opt_in_once(kern, BwdCfg<D>::kSmemBytes, opted_in);
   if (e != cudaSuccess) return e;
   int head_major = 1;
   if (kCausal && (e = causal_head_major(p, D, &head_major)) != cudaSuccess) return e;

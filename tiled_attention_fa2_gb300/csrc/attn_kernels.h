@@ -2,11 +2,28 @@
 // translation units.  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace attn {
+
+// Sets a kernel's dynamic shared-memory limit on the current device, once per
+// device: `done` (one per kernel instantiation) records the devices already
+// set (ordinals >= 64 are set on every call).  A repeated set from another
+// thread is harmless.
+template <class Kernel>
+cudaError_t smem_opt_in_once(Kernel kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Arguments of the tensor-core forward kernels (bf16 and e4m3 inputs).
 // Q, K, V are [B, H, N, d] row-major and reached only through the TMA
@@ -19,7 +36,10 @@ struct TcParams {
   void* o;              // bf16 [BH, N, d]
   float* lse;           // fp32 [BH, N], natural log
   int* status;          // device status word (timeouts)
-  int BH;               // B * H
+  int BH;               // B * H (query heads)
+  int H;                // query heads per batch entry
+  int kv_group;         // query heads per K/V head (grouped-query attention; 1 = multi-head):
+                        //   K/V are [B, H / kv_group, N, d] and query head h reads K/V head h / kv_group
   int N;                // sequence length (queries = keys)
   int n_pairs;          // ceil(N / 256): CTAs per head (two 128-row query tiles each)
   float scale_log2;     // softmax scale * log2(e) * q_descale * k_descale
@@ -54,9 +74,17 @@ struct SimtParams {
   float* o;
   float* lse;
   int BH;
+  int H;                // query heads per batch entry
+  int kv_group;         // query heads per K/V head (K/V are [B, H / kv_group, N, d])
   int N;
   float scale_log2;     // softmax scale * log2(e)
 };
+
+// K/V head (over B * H_kv) read by query head bh (over B * H) under grouped-query
+// attention: groups of kv_group consecutive query heads share one K/V head.
+__host__ __device__ __forceinline__ int kv_head_index(int bh, int H, int kv_group) {
+  return kv_group == 1 ? bh : (bh / H) * (H / kv_group) + (bh % H) / kv_group;
+}
 
 // Arguments of the backward kernels (bf16, d = 64 or 128).
 struct BwdParams {

@@ -11,10 +11,13 @@
 //
 // Limits and sharing rules (also stated in include/attn_fa2.h):
 //  * the array holds kNoAllocScratchBytes (64 MiB); larger plans are rejected;
-//  * every GPU that loads this library keeps the array until the process exits;
-//  * the first call on a device looks up the array's device address, once per
-//    device, with that device current -- make that first call before any
-//    stream capture;
+//  * CUDA loads this file's device code onto a device lazily, so the first
+//    call on a device is what commits the array there (and can fail with out
+//    of memory); it also looks up the array's device address, once per device,
+//    with that device current -- make that first call at set-up time, before
+//    any stream capture; the device then keeps the array until exit;
+//  * the address is cached per device ordinal, so cudaDeviceReset on a device
+//    while the library is in use there is not supported;
 //  * all calls share the array and it keeps the last call's contents; every
 //    byte a call reads it has written first, so nothing needs clearing; calls
 //    whose work overlaps on the GPU race on the array and must be serialised.

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_simt_f32_kernel(const SimtP
   const int off = (tid % TPR) * DPT;
   const bool live = row < N;
   const size_t head = static_cast<size_t>(bh) * N * D;
+  const size_t kv_head = static_cast<size_t>(kv_head_index(bh, p.H, p.kv_group)) * N * D;
 
   float q[DPT], o[DPT];
 #pragma unroll
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_simt_f32_kernel(const SimtP
     for (int e = tid; e < kKeyTile * D; e += kThreads) {
       const int r = e / D, c = e % D;
       const bool in = k0 + r < N;
-      const size_t g = head + static_cast<size_t>(k0 + r) * D + c;
+      const size_t g = kv_head + static_cast<size_t>(k0 + r) * D + c;
       sk[r][c] = in ? p.k[g] : 0.f;
       sv[r][c] = in ? p.v[g] : 0.f;
     }

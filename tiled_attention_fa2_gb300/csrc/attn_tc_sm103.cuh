@@ -65,7 +65,14 @@ struct TcCfg {
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kBarOff = kQBytes + kStages * kTileBytes;  // 2*kStages + 15 barriers + TMEM holder
   static constexpr int kSmemBytes = kBarOff + 1024 /*barriers*/ + 1024 /*alignment slack*/;
-  static constexpr int kThreads = 320;
+  // Non-causal: 384 threads with a register split (setmaxnreg) that gives the
+  // softmax warps 200 registers; causal: 320 threads at 168 (measured faster
+  // there: short items, where the extra warpgroup only adds set-up).
+  static constexpr bool kRegSplit = !kCausal;
+  static constexpr int kThreads = kRegSplit ? 384 : 320;
+  static constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104;
+  // setmaxnreg draws on the registers the block was launched with (168 each).
+  static_assert(!kRegSplit || 128 * kRegsOther + 256 * kRegsSoftmax <= 168 * kThreads, "register split too large");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol0 = 256;
 };
@@ -158,6 +165,15 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
   store_half<C, kHalf>(s, t_s);
 }
 
+// e4m3: the rounding error that storing a row's largest weight of a key tile
+// in P adds, e4m3(p_max) - p_max, with p_max computed exactly as the
+// exponential pass computes that key's weight (same FFMA, same ex2).
+template <class C>
+__device__ __forceinline__ float top_weight_rounding(float mx, float sl2, float neg_ref) {
+  const float p_max = ex2_approx(fmaf(mx, sl2, neg_ref));
+  return e4m3_round(p_max) - p_max;
+}
+
 // Optional event trace (compile with -DATTN_TRACE): per-CTA cycle stamps of
 // the pipeline hand-offs of one chosen CTA, for timeline analysis.
 #ifdef ATTN_TRACE
@@ -178,6 +194,7 @@ static __device__ unsigned long long g_attn_cta_span[8192 * 4];
 // Work item -> (b*h, pair of query tiles) and the key tiles each query tile visits.
 struct Item {
   int bh, pair, split;
+  int kv_bh;             // K/V head read by query head bh (differs from bh under grouped-query attention)
   int kv0;               // first key tile of the item's range
   int kv_end0, kv_end1;  // key tiles visited by query tile 0 / 1 (counted from kv0)
 };
@@ -204,6 +221,7 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int item, int n_k
     it.kv_end0 = min(n_kt - it.kv0, p.kt_per_split);
     it.kv_end1 = it.kv_end0;
   }
+  it.kv_bh = kv_head_index(it.bh, p.H, p.kv_group);
   return it;
 }
 
@@ -294,164 +312,173 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
   }
 #endif
 
-  if (warp == 8) {
-    // ================================================================ TMA producer
-    // The whole warp runs this loop; one elected lane issues each copy.  The
-    // K/V ring position `it` runs on across work items.
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-    }
-    __syncwarp();
-    int it = 0, nq = 0;
-    bool ok = true;
-    auto load_kv = [&](int k, const Item& w) -> bool {  // ring position `it` <- K_{k/2} (even k) or V_{k/2}
-      const int s = it % kS;
-      if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ((it / kS) & 1) ^ 1u, p.status, lim))) return false;
-      mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
-      const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
-      for (int b = 0; b < C::kBlocks; ++b)
-        tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
-                          (w.kv0 + (k >> 1)) * 128, w.bh);
-      ++it;
-      return true;
-    };
-    auto load_q = [&](int t, const Item& w) -> bool {
-      // Q_t's buffer is free once the previous item's last S_t = Q_t K^T completed.
-      if (nq > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty(t), (nq - 1) & 1, p.status, lim))) return false;
-      // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
-      // its results are never stored.
-      const int y = (2 * w.pair + t) * 128 < N ? (2 * w.pair + t) * 128 : 0;
-      mbar_arrive_expect_tx_elect(q_full(t), C::kTileBytes);
-      for (int b = 0; b < C::kBlocks; ++b)
-        tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full(t), b * C::kBoxCols, y,
-                          w.bh);
-      return true;
-    };
-    for (int r = 0; ok; ++r) {
-      const int item = item_of_round(r);
-      if (item >= total) break;
-      const Item w = decode_item<C>(p, item, n_kt);
-      ATTN_TRACE_EV(tr && lane == 0, 8, r, 0);
-      // Ring order: K_0, V_0, K_1, V_1, ...; Q_0 goes ahead of K_0 and Q_1 ahead of V_0,
-      // so the item's first S_0 = Q_0 K_0^T can start before the previous item's tile 1 is done.
-      ok = load_q(0, w) && load_kv(0, w) && load_q(1, w);
-      ++nq;
-      // Warm L2 with the next item's Q tiles and first K/V tiles.
-      const int nitem = item_of_round(r + 1);
-      if (ok && nitem < total) {
-        const Item nw = decode_item<C>(p, nitem, n_kt);
-        for (int t = 0; t < 2; ++t) {
-          const int y = (2 * nw.pair + t) * 128 < N ? (2 * nw.pair + t) * 128 : 0;
-          for (int b = 0; b < C::kBlocks; ++b) tma_prefetch_3d_elect(&p.tm_q, b * C::kBoxCols, y, nw.bh);
-        }
-        for (int b = 0; b < C::kBlocks; ++b) {
-          tma_prefetch_3d_elect(&p.tm_k, b * C::kBoxCols, nw.kv0 * 128, nw.bh);
-          tma_prefetch_3d_elect(&p.tm_v, b * C::kBoxCols, nw.kv0 * 128, nw.bh);
-        }
+  // Register split (non-causal instantiations, 384 threads): launched at 168
+  // registers per thread (384 x 168 = 64 512); warpgroup 2 (producer, MMA and two
+  // idle warps) drops to 104 and the softmax warpgroups rise to 200:
+  // 128 x 104 + 256 x 200 = 64 512.  Each warpgroup executes its setmaxnreg once,
+  // ahead of its role code.
+  if (warp >= 8) {
+    if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegsOther>();
+    if (warp == 8) {
+      // ================================================================ TMA producer
+      // The whole warp runs this loop; one elected lane issues each copy.  The
+      // K/V ring position `it` runs on across work items.
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
       }
-      for (int k = 1; ok && k < 2 * w.kv_end1; ++k) ok = load_kv(k, w);
-    }
-    // Drain: every copy this warp issued has landed before the CTA may exit.
-    for (int t = 0; nq > 0 && t < 2; ++t) mbar_wait(q_full(t), (nq - 1) & 1, p.status, lim);
-    for (int k = max(0, it - kS); k < it; ++k) mbar_wait(slot_full(k % kS), (k / kS) & 1, p.status, lim);
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
-    // Order per key tile j: for each query tile t, O_t += P_t V_j in two halves
-    // (each half as soon as the softmax has written it), then S_t = Q_t K_{j+1}^T
-    // into the same TMEM columns (tcgen05.mma issued by one thread executes in
-    // order, so the P_t reads precede the S_t overwrite).  The whole warp runs
-    // the loop; one elected lane issues every tcgen05 instruction.
-    auto wait_all = [&](uint32_t b, uint32_t par) {
-      return __all_sync(0xffffffffu, mbar_wait(b, par, p.status, lim));
-    };
-    int it = 0, nq = 0;
-    int np[2] = {0, 0};  // P tiles consumed per query tile (phase of p_lo / p_hi)
-    bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int item = item_of_round(r);
-      if (item >= total) break;
-      const Item w = decode_item<C>(p, item, n_kt);
-      ok = wait_all(q_full(0), nq & 1);
-      if (ok) ok = wait_all(slot_full(it % kS), (it / kS) & 1);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const uint32_t kb = slot_base + (it % kS) * C::kTileBytes;
-        issue_qk<C>(tmem + 0, q_base, kb);
-        mma_commit_elect(s_full(0));
-        if (w.kv_end0 == 1) mma_commit_elect(q_empty(0));  // the item's last use of Q_0
-        ok = wait_all(q_full(1), nq & 1);
+      __syncwarp();
+      int it = 0, nq = 0;
+      bool ok = true;
+      auto load_kv = [&](int k, const Item& w) -> bool {  // ring position `it` <- K_{k/2} (even k) or V_{k/2}
+        const int s = it % kS;
+        if (!__all_sync(0xffffffffu, mbar_wait(slot_empty(s), ((it / kS) & 1) ^ 1u, p.status, lim))) return false;
+        mbar_arrive_expect_tx_elect(slot_full(s), C::kTileBytes);
+        const CUtensorMap* map = (k & 1) ? &p.tm_v : &p.tm_k;
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d_elect(slot_base + s * C::kTileBytes + b * C::kBlockBytes, map, slot_full(s), b * C::kBoxCols,
+                            (w.kv0 + (k >> 1)) * 128, w.kv_bh);
+        ++it;
+        return true;
+      };
+      auto load_q = [&](int t, const Item& w) -> bool {
+        // Q_t's buffer is free once the previous item's last S_t = Q_t K^T completed.
+        if (nq > 0 && !__all_sync(0xffffffffu, mbar_wait(q_empty(t), (nq - 1) & 1, p.status, lim))) return false;
+        // A query tile wholly past N (odd tile count) loads rows 0..127 instead;
+        // its results are never stored.
+        const int y = (2 * w.pair + t) * 128 < N ? (2 * w.pair + t) * 128 : 0;
+        mbar_arrive_expect_tx_elect(q_full(t), C::kTileBytes);
+        for (int b = 0; b < C::kBlocks; ++b)
+          tma_load_3d_elect(q_base + t * C::kTileBytes + b * C::kBlockBytes, &p.tm_q, q_full(t), b * C::kBoxCols, y,
+                            w.bh);
+        return true;
+      };
+      for (int r = 0; ok; ++r) {
+        const int item = item_of_round(r);
+        if (item >= total) break;
+        const Item w = decode_item<C>(p, item, n_kt);
+        ATTN_TRACE_EV(tr && lane == 0, 8, r, 0);
+        // Ring order: K_0, V_0, K_1, V_1, ...; Q_0 goes ahead of K_0 and Q_1 ahead of V_0,
+        // so the item's first S_0 = Q_0 K_0^T can start before the previous item's tile 1 is done.
+        ok = load_q(0, w) && load_kv(0, w) && load_q(1, w);
+        ++nq;
+        // Warm L2 with the next item's Q tiles and first K/V tiles.
+        const int nitem = item_of_round(r + 1);
+        if (ok && nitem < total) {
+          const Item nw = decode_item<C>(p, nitem, n_kt);
+          for (int t = 0; t < 2; ++t) {
+            const int y = (2 * nw.pair + t) * 128 < N ? (2 * nw.pair + t) * 128 : 0;
+            for (int b = 0; b < C::kBlocks; ++b) tma_prefetch_3d_elect(&p.tm_q, b * C::kBoxCols, y, nw.bh);
+          }
+          for (int b = 0; b < C::kBlocks; ++b) {
+            tma_prefetch_3d_elect(&p.tm_k, b * C::kBoxCols, nw.kv0 * 128, nw.kv_bh);
+            tma_prefetch_3d_elect(&p.tm_v, b * C::kBoxCols, nw.kv0 * 128, nw.kv_bh);
+          }
+        }
+        for (int k = 1; ok && k < 2 * w.kv_end1; ++k) ok = load_kv(k, w);
+      }
+      // Drain: every copy this warp issued has landed before the CTA may exit.
+      for (int t = 0; nq > 0 && t < 2; ++t) mbar_wait(q_full(t), (nq - 1) & 1, p.status, lim);
+      for (int k = max(0, it - kS); k < it; ++k) mbar_wait(slot_full(k % kS), (k / kS) & 1, p.status, lim);
+    } else if (warp == 9) {
+      // ================================================================ MMA issuer
+      // Order per key tile j: for each query tile t, O_t += P_t V_j in two halves
+      // (each half as soon as the softmax has written it), then S_t = Q_t K_{j+1}^T
+      // into the same TMEM columns (tcgen05.mma issued by one thread executes in
+      // order, so the P_t reads precede the S_t overwrite).  The whole warp runs
+      // the loop; one elected lane issues every tcgen05 instruction.
+      auto wait_all = [&](uint32_t b, uint32_t par) {
+        return __all_sync(0xffffffffu, mbar_wait(b, par, p.status, lim));
+      };
+      int it = 0, nq = 0;
+      int np[2] = {0, 0};  // P tiles consumed per query tile (phase of p_lo / p_hi)
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int item = item_of_round(r);
+        if (item >= total) break;
+        const Item w = decode_item<C>(p, item, n_kt);
+        ok = wait_all(q_full(0), nq & 1);
+        if (ok) ok = wait_all(slot_full(it % kS), (it / kS) & 1);
         if (!ok) break;
         tc_fence_after();
-        issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
-        mma_commit_elect(s_full(1));
-        if (w.kv_end1 == 1) mma_commit_elect(q_empty(1));
-        mma_commit_elect(slot_empty(it % kS));
-        ++it;
-        ATTN_TRACE_EV(tr && lane == 0, 8, r, 1);
-      }
-      for (int j = 0; ok && j < w.kv_end1; ++j) {
-        const int sv = it % kS;
-        ok = wait_all(slot_full(sv), (it / kS) & 1);
-        if (!ok) break;
-        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2, j, 4);
-        const int itk = it + 1;
-        const int sk = itk % kS;
-        const bool next = (j + 1 < w.kv_end1);
-        bool k_ready = false;
-        const uint32_t v_addr = slot_base + sv * C::kTileBytes;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int kv_end = t ? w.kv_end1 : w.kv_end0;
-          if (j < kv_end) {
-            // The first O_t += P_t V of an item overwrites O_t: the previous
-            // item's epilogue must have read it out.
-            if (j == 0 && nq > 0) {
-              ok = wait_all(o_empty(t), (nq - 1) & 1);
-              if (!ok) break;
-            }
-            ok = wait_all(p_lo(t), np[t] & 1);
-            if (!ok) break;
-            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 0);
-            tc_fence_after();
-            issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
-            ok = wait_all(p_hi(t), np[t] & 1);
-            if (!ok) break;
-            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 1);
-            tc_fence_after();
-            issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
-            ++np[t];
-            // O_t is read only after its last P.V of the item; earlier rescales
-            // rely on S_{j+1} completing after P_j V_j instead.
-            if (j == kv_end - 1) mma_commit_elect(o_full(t));
-            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 2);
-          }
-          if (t == 1) mma_commit_elect(slot_empty(sv));
-          if (j + 1 < kv_end) {
-            if (!k_ready) {
-              ok = wait_all(slot_full(sk), (itk / kS) & 1);
-              if (!ok) break;
-              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 5);
-              tc_fence_after();
-              k_ready = true;
-            }
-            issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
-            mma_commit_elect(s_full(t));
-            if (j + 2 == kv_end) mma_commit_elect(q_empty(t));  // the item's last S_t = Q_t K^T
-            ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
-          }
+        {
+          const uint32_t kb = slot_base + (it % kS) * C::kTileBytes;
+          issue_qk<C>(tmem + 0, q_base, kb);
+          mma_commit_elect(s_full(0));
+          if (w.kv_end0 == 1) mma_commit_elect(q_empty(0));  // the item's last use of Q_0
+          ok = wait_all(q_full(1), nq & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
+          mma_commit_elect(s_full(1));
+          if (w.kv_end1 == 1) mma_commit_elect(q_empty(1));
+          mma_commit_elect(slot_empty(it % kS));
+          ++it;
+          ATTN_TRACE_EV(tr && lane == 0, 8, r, 1);
         }
-        if (!ok) break;
-        if (next) mma_commit_elect(slot_empty(sk));
-        it += next ? 2 : 1;  // V_j, and K_{j+1} if this item has one (the producer loads 2 per key tile)
+        for (int j = 0; ok && j < w.kv_end1; ++j) {
+          const int sv = it % kS;
+          ok = wait_all(slot_full(sv), (it / kS) & 1);
+          if (!ok) break;
+          ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2, j, 4);
+          const int itk = it + 1;
+          const int sk = itk % kS;
+          const bool next = (j + 1 < w.kv_end1);
+          bool k_ready = false;
+          const uint32_t v_addr = slot_base + sv * C::kTileBytes;
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int kv_end = t ? w.kv_end1 : w.kv_end0;
+            if (j < kv_end) {
+              // The first O_t += P_t V of an item overwrites O_t: the previous
+              // item's epilogue must have read it out.
+              if (j == 0 && nq > 0) {
+                ok = wait_all(o_empty(t), (nq - 1) & 1);
+                if (!ok) break;
+              }
+              ok = wait_all(p_lo(t), np[t] & 1);
+              if (!ok) break;
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 0);
+              tc_fence_after();
+              issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
+              ok = wait_all(p_hi(t), np[t] & 1);
+              if (!ok) break;
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 1);
+              tc_fence_after();
+              issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
+              ++np[t];
+              // O_t is read only after its last P.V of the item; earlier rescales
+              // rely on S_{j+1} completing after P_j V_j instead.
+              if (j == kv_end - 1) mma_commit_elect(o_full(t));
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 2);
+            }
+            if (t == 1) mma_commit_elect(slot_empty(sv));
+            if (j + 1 < kv_end) {
+              if (!k_ready) {
+                ok = wait_all(slot_full(sk), (itk / kS) & 1);
+                if (!ok) break;
+                ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 5);
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
+              mma_commit_elect(s_full(t));
+              if (j + 2 == kv_end) mma_commit_elect(q_empty(t));  // the item's last S_t = Q_t K^T
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
+            }
+          }
+          if (!ok) break;
+          if (next) mma_commit_elect(slot_empty(sk));
+          it += next ? 2 : 1;  // V_j, and K_{j+1} if this item has one (the producer loads 2 per key tile)
+        }
+        ++nq;
       }
-      ++nq;
+      // Every MMA issued by this warp has completed before TMEM is freed.
+      mma_commit_elect(mma_done);
+      mbar_wait(mma_done, 0, p.status, lim);
     }
-    // Every MMA issued by this warp has completed before TMEM is freed.
-    mma_commit_elect(mma_done);
-    mbar_wait(mma_done, 0, p.status, lim);
   } else {
+    if constexpr (C::kRegSplit) setmaxnreg_inc<C::kRegsSoftmax>();
     // ================================================================ softmax warpgroups
     const int t = tid >> 7;                      // query tile of this warpgroup
     const int r = tid & 127;                     // row inside the tile = TMEM lane
@@ -473,7 +500,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       const int row = qt * 128 + r;
       const int kv_end = t ? w.kv_end1 : w.kv_end0;
       float m2 = -INFINITY;  // reference max of s * sl2 (log2 domain)
-      float l = 0.f;         // running sum of p * 2^kPExp
+      float l = 0.f;         // running sum of p * 2^kPExp (fp32 p: gives L)
+      float lc = 0.f;        // e4m3: running sum of the rounding errors of each key tile's largest weight
 
       for (int j = 0; j < kv_end; ++j, ++ns) {
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), ns & 1, p.status, lim));
@@ -482,22 +510,47 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         ATTN_TRACE_EV(trw && j == 0, 8, rr, 2 + 3 * t);
         ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 4, j, t * 4 + (warp & 3));
         tc_fence_after();
-        uint32_t u[128];
-        tmem_ld128_sync(t_s, u);
-        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 6, j, t * 4 + (warp & 3));
+        // Keys 0..63 are loaded first; the load of keys 64..127 stays in flight
+        // while the first half is masked and reduced (and, after the first key
+        // tile, exponentiated).
+        // (bf16 only: the e4m3 step keeps more values live across that window
+        // than the registers hold, and it loads all 128 columns at once.)
+        uint32_t ua[64], ub[64];
         float s[128];
+        if constexpr (C::kIsFp8) {
+          uint32_t u[128];
+          tmem_ld128_sync(t_s, u);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
+        } else {
+          tmem_ld64_then_ld64(t_s, ua, t_s + 64, ub);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(ua[c]);
+        }
+        ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 6, j, t * 4 + (warp & 3));
         const int jj = w.kv0 + j;  // absolute key tile
         const bool diag = C::kCaus && (jj == qt);
         const bool ragged = (jj == n_kt - 1) && ((N & 127) != 0);
+        const int key0 = jj * 128;
+        const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
         if (diag || ragged) {
-          const int key0 = jj * 128;
-          const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
+          for (int c = 0; c < (C::kIsFp8 ? 128 : 64); ++c)
             if (key0 + c > lim_key) s[c] = -INFINITY;
         }
+        // The second half (bf16): waited for, converted and masked by land_hi().
+        auto land_hi = [&]() {
+          if constexpr (!C::kIsFp8) {
+            tmem_wait_ld_dep(ub);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(ub[c]);
+            if (diag || ragged) {
+#pragma unroll
+              for (int c = 64; c < 128; ++c)
+                if (key0 + c > lim_key) s[c] = -INFINITY;
+            }
+          }
+        };
         // Fast path (e4m3, every key tile after the first): with the drift bound
         // of 4 doublings the reference max rarely moves, so the exponentials of
         // keys 0..63 are computed with the current reference while the same pass
@@ -514,8 +567,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
           for (int c = 0; c < 64; c += 4) {
             ma = fmax3(ma, s[c], s[c + 1]);
             mb = fmax3(mb, s[c + 2], s[c + 3]);
-            mc = fmax3(mc, s[64 + c], s[64 + c + 1]);
-            md = fmax3(md, s[64 + c + 2], s[64 + c + 3]);
             const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, neg_ref);
             const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, neg_ref);
             s[c] = ex2_approx(f2_lo(a));
@@ -524,6 +575,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
             s[c + 3] = ex2_approx(f2_hi(b));
             rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
             rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
+          }
+          land_hi();
+#pragma unroll
+          for (int c = 64; c < 128; c += 4) {
+            mc = fmax3(mc, s[c], s[c + 1]);
+            md = fmax3(md, s[c + 2], s[c + 3]);
           }
           const float mx = fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
           fast = !__any_sync(0xffffffffu, mx * sl2 > m2 + C::kTau);
@@ -542,6 +599,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
             ATTN_TRACE_EV(trw && nq == 0, t, j, 3);
             const uint64_t rs = f2_add(rs0, rs1);
             l += f2_lo(rs) + f2_hi(rs);
+            lc += top_weight_rounding<C>(mx, sl2, C::kPExp - m2);
             continue;
           }
           // Slow path: reload the raw scores of keys 0..63 and mask them again.
@@ -565,6 +623,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
         for (int c = 16; c < 128; c += 16) {
+          // keys 64..127 arrive here (the e4m3 guess above has landed them already)
+          if (c == 64 && !(C::kIsFp8 && j > 0)) land_hi();
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
             mx8[i] = fmax3(mx8[i], s[c + i], s[c + i + 1]);
@@ -614,6 +674,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         ATTN_TRACE_EV(trw && nq == 0, t, j, 3);
         const uint64_t rs = f2_add(rs0, rs1);
         l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
+        if constexpr (C::kIsFp8) lc = fmaf(lc, alpha, top_weight_rounding<C>(mx, sl2, C::kPExp - m_use));
         m2 = m_new;
       }
       if (!ok) break;
@@ -629,7 +690,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty(t));
-      const float inv = p.o_scale / l;
+      // e4m3: P.V accumulated the rounded codes of P while l sums the fp32
+      // weights.  On a peaked row one weight carries most of the sum, and its
+      // rounding (relative error up to 2^-4) would scale O by as much; the
+      // normaliser of O therefore adds back each key tile's largest-weight
+      // rounding error, so a row's dominant weight divides out exactly.  L keeps
+      // the fp32 sum, which has none of that rounding.
+      const float inv = p.o_scale / (C::kIsFp8 ? l + lc : l);
       const float lse_v = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       if (row < N) {
         if (p.part_o != nullptr) {
@@ -678,7 +745,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
 template <class C>
 cudaError_t launch_tc(const TcParams& p, int num_sms, cudaStream_t stream) {
   auto kern = attn_fwd_tc_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static std::atomic<unsigned long long> opted_in{0};
+  cudaError_t e = smem_opt_in_once(kern, C::kSmemBytes, opted_in);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
   const long long grid = items < num_sms ? items : num_sms;  // persistent: at most one CTA per SM

@@ -20,12 +20,16 @@ import torch
 E4M3_MAX = 448.0  # largest finite magnitude of FP8 E4M3 ("fn" variant)
 
 
-def make_qkv_f32(B: int, H: int, N: int, d: int, seed: int = 0, q_mult: float = 1.0):
-    """Float32 Q, K, V drawn i.i.d. N(0, 1) on the CPU, in the order Q, K, V."""
+def make_qkv_f32(B: int, H: int, N: int, d: int, seed: int = 0, q_mult: float = 1.0, n_kv_heads: int | None = None):
+    """Float32 Q, K, V drawn i.i.d. N(0, 1) on the CPU, in the order Q, K, V.
+
+    Q is [B, H, N, d]; K and V are [B, n_kv_heads, N, d] (default H heads; fewer
+    for grouped-query attention)."""
+    hkv = H if n_kv_heads is None else int(n_kv_heads)
     g = torch.Generator(device="cpu").manual_seed(int(seed))
     q = torch.randn((B, H, N, d), dtype=torch.float32, generator=g)
-    k = torch.randn((B, H, N, d), dtype=torch.float32, generator=g)
-    v = torch.randn((B, H, N, d), dtype=torch.float32, generator=g)
+    k = torch.randn((B, hkv, N, d), dtype=torch.float32, generator=g)
+    v = torch.randn((B, hkv, N, d), dtype=torch.float32, generator=g)
     if q_mult != 1.0:
         q = q * float(q_mult)
     return q, k, v
@@ -88,7 +92,8 @@ def sample_rows(N: int, B: int, H: int, count: int = 512) -> np.ndarray:
 
 
 # Named workloads: the sizes and element types the library is checked and
-# measured on.  ``name -> dict(B, H, N, d, dtype, causal, q_mult)``.
+# measured on.  ``name -> dict(B, H, N, d, dtype, causal, q_mult[, Hkv])``;
+# ``Hkv`` (K/V heads, grouped-query attention) defaults to H.
 WORKLOADS = {
     "tiny_f32": dict(B=1, H=2, N=256, d=64, dtype="f32", causal=False, q_mult=1.0),
     "prefill_causal_bf16": dict(B=4, H=16, N=2048, d=128, dtype="bf16", causal=True, q_mult=1.0),
@@ -99,6 +104,10 @@ WORKLOADS = {
     "dit_e4m3": dict(B=1, H=56, N=30272, d=128, dtype="e4m3", causal=False, q_mult=1.0),
     "long_causal_bf16": dict(B=1, H=8, N=32768, d=128, dtype="bf16", causal=True, q_mult=1.0),
     "long_causal_e4m3": dict(B=1, H=8, N=32768, d=128, dtype="e4m3", causal=True, q_mult=1.0),
+    # Grouped-query attention at the head counts of a Llama-3-70B-class model
+    # (64 query heads sharing 8 K/V heads, d = 128), causal prefill of 8192 tokens.
+    "prefill_gqa_bf16": dict(B=1, H=64, Hkv=8, N=8192, d=128, dtype="bf16", causal=True, q_mult=1.0),
+    "prefill_gqa_e4m3": dict(B=1, H=64, Hkv=8, N=8192, d=128, dtype="e4m3", causal=True, q_mult=1.0),
 }
 
 
