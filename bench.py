@@ -51,8 +51,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # The sources the tensor-core forward kernel and its launch are built from; a
 # change anywhere else (backward, fp32 path, split-KV merge) leaves it as it was.
-FWD_SOURCES = ("attn_api.cu", "attn_kernels.h", "attn_tc_bf16.cu", "attn_tc_e4m3.cu", "attn_tc_sm103.cuh",
-               "ptx_sm103.cuh")
+FWD_SOURCES = ("attn_api.cu", "attn_kernels.h", "attn_tc_bf16.cu", "attn_tc_e4m3.cu", "attn_tc_e4m3_poly.cu",
+               "attn_tc_sm103.cuh", "exp2_poly.h", "ptx_sm103.cuh")
 
 
 def kernel_source_hash(files=FWD_SOURCES) -> str:

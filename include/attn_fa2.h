@@ -203,6 +203,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  */
 int attn_get_device_status(void* stream);
 
+/*
+ * Split exponential for the e4m3 forward ("Kernels and Memory in LLM
+ * Inference", "FlashAttention-4: when the roof moves", item 1: a short
+ * polynomial on the CUDA cores computes some exponentials while the
+ * exponential unit computes the rest).  on = 1: later e4m3 launches from this
+ * process evaluate one exponential pair in four with a degree-3 polynomial on
+ * the FMA pipe (max relative error 7.5e-5; exp2_poly.h); on = 0 (the default):
+ * every exponential on the exponential unit.  Returns the previous setting, or
+ * -1 (nothing changed) for any other value of on.  A tuning knob: results stay
+ * within the stated tolerances either way.
+ */
+int attn_set_poly_exp2(int on);
+
 /* Upper bound (nanoseconds, >= 1e6) on any single device-side wait of later
  * launches from this process; default 2e9 (2 s).  Returns the previous value. */
 uint64_t attn_set_wait_limit_ns(uint64_t ns);

@@ -23,7 +23,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libattn_fa2.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "obj")
 
-SOURCES = ["attn_api.cu", "attn_simt_f32.cu", "attn_tc_bf16.cu", "attn_tc_e4m3.cu", "attn_split_combine.cu", "attn_noalloc.cu", "attn_bwd.cu"]
+SOURCES = ["attn_api.cu", "attn_simt_f32.cu", "attn_tc_bf16.cu", "attn_tc_e4m3.cu", "attn_tc_e4m3_poly.cu", "attn_split_combine.cu", "attn_noalloc.cu", "attn_bwd.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -30,6 +30,7 @@ SIGNATURES = {
     "attn_fwd_host": (_I, [_VP] * 10 + [_I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _VP]),
     "attn_get_device_status": (_I, [_VP]),
     "attn_set_wait_limit_ns": (_U64, [_U64]),
+    "attn_set_poly_exp2": (_I, [_I]),
     "attn_selftest_wait_timeout": (_I, [_U64, _VP]),
     "attn_fwd_split_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
     "attn_fwd_split": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _I, _VP, ctypes.c_size_t,
@@ -313,3 +314,12 @@ def forward(q, k, v, causal=False, scale=None, descales=None):
     if _dtype_code(q) == ATTN_E4M3 and descales is not None:
         return attn_fwd_fp8(q, k, v, *descales, scale=scale, causal=causal)
     return attn_fwd(q, k, v, scale=scale, causal=causal)
+
+
+def set_poly_exp2(on: bool) -> bool:
+    """Split exponential for the e4m3 forward (one exponential pair in four by a
+    polynomial on the FMA pipe); returns the previous setting."""
+    prev = load_library().attn_set_poly_exp2(int(bool(on)))
+    if prev < 0:
+        raise ValueError("attn_set_poly_exp2 refused the setting")
+    return bool(prev)

@@ -1,6 +1,7 @@
 // C-ABI layer of libattn_fa2.so: argument validation, TMA descriptor encoding,
 // kernel selection and launch, device status word.  The entry points are
 // declared (with their contracts) in include/attn_fa2.h.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -23,6 +24,7 @@ __device__ int g_attn_status = 0;
 
 thread_local char g_last_error[256] = "";
 uint64_t g_wait_limit_ns = 2000000000ull;
+std::atomic<int> g_poly_exp2{0};  // attn_set_poly_exp2
 
 int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int status, const char* fmt, ...) {
@@ -229,8 +231,9 @@ int run_tc(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (n_pairs * BH * n_splits > 0x7fffffffLL) return fail(ATTN_ERR_UNSUPPORTED, "too many work items");
   int sms = 0;
   if ((st = num_sms(&sms)) != ATTN_OK) return st;
-  cudaError_t e = fp8 ? attn::launch_tc_e4m3(p, d, causal != 0, sms, stream)
-                      : attn::launch_tc_bf16(p, d, causal != 0, sms, stream);
+  cudaError_t e = !fp8 ? attn::launch_tc_bf16(p, d, causal != 0, sms, stream)
+                 : g_poly_exp2.load(std::memory_order_relaxed) ? attn::launch_tc_e4m3_poly(p, d, causal != 0, sms, stream)
+                                                               : attn::launch_tc_e4m3(p, d, causal != 0, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ATTN_OK;
 }
@@ -527,6 +530,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   cudaError_t e = attn::launch_bwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ATTN_OK;
+}
+
+int attn_set_poly_exp2(int on) {
+  if (on != 0 && on != 1) return -1;
+  return g_poly_exp2.exchange(on);
 }
 
 uint64_t attn_set_wait_limit_ns(uint64_t ns) {

@@ -115,6 +115,8 @@ struct BwdParams {
 // The tensor-core kernels are persistent: min(#work items, num_sms) CTAs.
 cudaError_t launch_tc_bf16(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_tc_e4m3(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
+// e4m3 with the split exponential (one exponential pair in four by polynomial).
+cudaError_t launch_tc_e4m3_poly(const TcParams& p, int d, bool causal, int num_sms, cudaStream_t stream);
 cudaError_t launch_simt_f32(const SimtParams& p, int d, bool causal, cudaStream_t stream);
 cudaError_t launch_split_combine(const CombineParams& p, int d, cudaStream_t stream);
 // Backward: D and the zeroed dQ accumulator, the tensor-core pass, dQ to bf16.

@@ -33,9 +33,14 @@
 
 namespace attn {
 
-template <bool kFp8, int kD, bool kCausal>
+template <bool kFp8, int kD, bool kCausal, bool kPolyExp2 = false>
 struct TcCfg {
   static constexpr bool kIsFp8 = kFp8;
+  // Split exponential ("Kernels and Memory in LLM Inference", FlashAttention-4
+  // section, item 1): when set, one exponential pair in four is evaluated by
+  // the polynomial of exp2_poly.h on the FMA pipe instead of the exponential
+  // unit.  An option (attn_set_poly_exp2), off by default.
+  static constexpr bool kPoly = kPolyExp2;
   static constexpr int D = kD;
   static constexpr bool kCaus = kCausal;
   static constexpr int kElem = kFp8 ? 1 : 2;                 // bytes per element
@@ -50,14 +55,15 @@ struct TcCfg {
   static constexpr int kPvSteps = 128 / kMmaK;
   static constexpr int kStages = (kTileBytes == 32768) ? 5 : 8;
   static constexpr int kPCols = kFp8 ? 32 : 64;              // TMEM columns of one P tile
-  // Conditional rescale: the reference max used in the exponentials moves only
+  // Conditional rescale ("Kernels and Memory in LLM Inference", FlashAttention-4
+  // section, item 2): the reference max used in the exponentials moves only
   // when the row max grows by more than kTau (log2 units), so p <= 2^kTau.
-  // P is stored as p * 2^kPExp; for e4m3 2^(kTau + kPExp) = 256 <= 448 (max finite).
-  // A stale reference leaves the dominant weight of a row at 2^x with x in
-  // (0, kTau], which bf16 rounds (while l sums the unrounded p); on strongly
-  // peaked rows that error reaches O itself, so bf16 keeps the drift to one
-  // doubling.  The e4m3 rounding of P dominates anyway, hence 4 there.
-  static constexpr float kTau = kFp8 ? 4.f : 1.f;
+  // P is stored as p * 2^kPExp; for e4m3 2^(kTau + kPExp) = 256 <= 448 (max
+  // finite).  A stale reference leaves a row's dominant weight at 2^x, x in
+  // (0, kTau], which the P format rounds while l sums the unrounded p; the
+  // normaliser of O adds that rounding back (top_weight_rounding), so the drift
+  // costs no accuracy.
+  static constexpr float kTau = kFp8 ? 4.f : 8.f;
   static constexpr float kPExp = kFp8 ? 4.f : 0.f;
   static constexpr uint32_t kFmt = kFp8 ? 0u : 1u;
   static constexpr uint32_t kIdescQK = make_idesc(kFmt, 128, 128, 0, 0);
@@ -122,6 +128,24 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 
 // Exponentials of keys [64h, 64h + 64) of this thread's score row, in place,
 // and their packed row sums.
+// Exponentials of one packed pair of exponents (log2 units), in place into
+// s[c], s[c + 1]: the exponential unit, or (pairs the split-exponential option
+// selects) the polynomial on the FMA pipe.  Pair k of a 64-key half is
+// polynomial when C::kPoly and k % 4 == 0.
+template <class C>
+__device__ __forceinline__ void exp2_pair(uint64_t x2, float& lo, float& hi, int pair) {
+  if (C::kPoly && (pair & 3) == 0) {
+    const uint64_t y = exp2_poly_x2(x2);
+    lo = f2_lo(y);
+    hi = f2_hi(y);
+  } else {
+    lo = ex2_approx(f2_lo(x2));
+    hi = ex2_approx(f2_hi(x2));
+  }
+}
+
+// Exponentials of keys [64h, 64h + 64) of this thread's score row, in place,
+// and their packed row sums.
 template <class C, int kHalf>
 __device__ __forceinline__ void exp_half(float (&s)[128], uint64_t sl2x2, uint64_t negx2, uint64_t& rs0,
                                          uint64_t& rs1) {
@@ -129,10 +153,8 @@ __device__ __forceinline__ void exp_half(float (&s)[128], uint64_t sl2x2, uint64
   for (int c = 64 * kHalf; c < 64 * kHalf + 64; c += 4) {
     const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, negx2);
     const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, negx2);
-    s[c] = ex2_approx(f2_lo(a));
-    s[c + 1] = ex2_approx(f2_hi(a));
-    s[c + 2] = ex2_approx(f2_lo(b));
-    s[c + 3] = ex2_approx(f2_hi(b));
+    exp2_pair<C>(a, s[c], s[c + 1], c / 2);
+    exp2_pair<C>(b, s[c + 2], s[c + 3], c / 2 + 1);
     rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
     rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
   }
@@ -165,13 +187,14 @@ __device__ __forceinline__ void softmax_half(float (&s)[128], uint64_t sl2x2, ui
   store_half<C, kHalf>(s, t_s);
 }
 
-// e4m3: the rounding error that storing a row's largest weight of a key tile
-// in P adds, e4m3(p_max) - p_max, with p_max computed exactly as the
-// exponential pass computes that key's weight (same FFMA, same ex2).
+// The rounding error that storing a row's largest weight of a key tile in P
+// adds (e4m3 or bf16, as store_half rounds it), with p_max computed exactly as
+// the exponential pass computes that key's weight (same FFMA, same ex2).
 template <class C>
 __device__ __forceinline__ float top_weight_rounding(float mx, float sl2, float neg_ref) {
   const float p_max = ex2_approx(fmaf(mx, sl2, neg_ref));
-  return e4m3_round(p_max) - p_max;
+  if constexpr (C::kIsFp8) return e4m3_round(p_max) - p_max;
+  else return __bfloat162float(__float2bfloat16_rn(p_max)) - p_max;
 }
 
 // Optional event trace (compile with -DATTN_TRACE): per-CTA cycle stamps of
@@ -501,7 +524,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       const int kv_end = t ? w.kv_end1 : w.kv_end0;
       float m2 = -INFINITY;  // reference max of s * sl2 (log2 domain)
       float l = 0.f;         // running sum of p * 2^kPExp (fp32 p: gives L)
-      float lc = 0.f;        // e4m3: running sum of the rounding errors of each key tile's largest weight
+      float lc = 0.f;        // running sum of the P rounding errors of each key tile's largest weight
 
       for (int j = 0; j < kv_end; ++j, ++ns) {
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), ns & 1, p.status, lim));
@@ -510,22 +533,12 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         ATTN_TRACE_EV(trw && j == 0, 8, rr, 2 + 3 * t);
         ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 4, j, t * 4 + (warp & 3));
         tc_fence_after();
-        // Keys 0..63 are loaded first; the load of keys 64..127 stays in flight
-        // while the first half is masked and reduced (and, after the first key
-        // tile, exponentiated).
-        // (bf16 only: the e4m3 step keeps more values live across that window
-        // than the registers hold, and it loads all 128 columns at once.)
-        uint32_t ua[64], ub[64];
         float s[128];
-        if constexpr (C::kIsFp8) {
+        {
           uint32_t u[128];
           tmem_ld128_sync(t_s, u);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c]);
-        } else {
-          tmem_ld64_then_ld64(t_s, ua, t_s + 64, ub);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(ua[c]);
         }
         ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 6, j, t * 4 + (warp & 3));
         const int jj = w.kv0 + j;  // absolute key tile
@@ -535,32 +548,18 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         const int lim_key = C::kCaus ? min(N - 1, row) : (N - 1);
         if (diag || ragged) {
 #pragma unroll
-          for (int c = 0; c < (C::kIsFp8 ? 128 : 64); ++c)
+          for (int c = 0; c < 128; ++c)
             if (key0 + c > lim_key) s[c] = -INFINITY;
         }
-        // The second half (bf16): waited for, converted and masked by land_hi().
-        auto land_hi = [&]() {
-          if constexpr (!C::kIsFp8) {
-            tmem_wait_ld_dep(ub);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(ub[c]);
-            if (diag || ragged) {
-#pragma unroll
-              for (int c = 64; c < 128; ++c)
-                if (key0 + c > lim_key) s[c] = -INFINITY;
-            }
-          }
-        };
-        // Fast path (e4m3, every key tile after the first): with the drift bound
-        // of 4 doublings the reference max rarely moves, so the exponentials of
+        // Fast path (every key tile after the first): with the drift bound of
+        // kTau doublings the reference max rarely moves, so the exponentials of
         // keys 0..63 are computed with the current reference while the same pass
         // finds the row max; only if some row of the warp grew past the bound is
         // the tile redone on the exact path below (S is still intact in TMEM: P
-        // has not been written yet).  bf16 keeps a bound of one doubling, which
-        // some row of a warp exceeds too often for the guess to pay.
+        // has not been written yet).
         uint64_t rs0 = 0, rs1 = 0;  // packed partial row sums (0 bits == 0.0f)
         bool fast = false;
-        if (C::kIsFp8 && j > 0) {
+        if (j > 0) {
           const uint64_t neg_ref = f2_pack(C::kPExp - m2, C::kPExp - m2);
           float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
 #pragma unroll
@@ -569,14 +568,11 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
             mb = fmax3(mb, s[c + 2], s[c + 3]);
             const uint64_t a = f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, neg_ref);
             const uint64_t b = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, neg_ref);
-            s[c] = ex2_approx(f2_lo(a));
-            s[c + 1] = ex2_approx(f2_hi(a));
-            s[c + 2] = ex2_approx(f2_lo(b));
-            s[c + 3] = ex2_approx(f2_hi(b));
+            exp2_pair<C>(a, s[c], s[c + 1], c / 2);
+            exp2_pair<C>(b, s[c + 2], s[c + 3], c / 2 + 1);
             rs0 = f2_add(rs0, f2_pack(s[c], s[c + 1]));
             rs1 = f2_add(rs1, f2_pack(s[c + 2], s[c + 3]));
           }
-          land_hi();
 #pragma unroll
           for (int c = 64; c < 128; c += 4) {
             mc = fmax3(mc, s[c], s[c + 1]);
@@ -623,8 +619,6 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
         for (int c = 16; c < 128; c += 16) {
-          // keys 64..127 arrive here (the e4m3 guess above has landed them already)
-          if (c == 64 && !(C::kIsFp8 && j > 0)) land_hi();
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
             mx8[i] = fmax3(mx8[i], s[c + i], s[c + i + 1]);
@@ -674,7 +668,7 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         ATTN_TRACE_EV(trw && nq == 0, t, j, 3);
         const uint64_t rs = f2_add(rs0, rs1);
         l = fmaf(l, alpha, f2_lo(rs) + f2_hi(rs));
-        if constexpr (C::kIsFp8) lc = fmaf(lc, alpha, top_weight_rounding<C>(mx, sl2, C::kPExp - m_use));
+        lc = fmaf(lc, alpha, top_weight_rounding<C>(mx, sl2, C::kPExp - m_use));
         m2 = m_new;
       }
       if (!ok) break;
@@ -690,13 +684,13 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty(t));
-      // e4m3: P.V accumulated the rounded codes of P while l sums the fp32
+      // P.V accumulated the rounded P (e4m3 or bf16) while l sums the fp32
       // weights.  On a peaked row one weight carries most of the sum, and its
-      // rounding (relative error up to 2^-4) would scale O by as much; the
-      // normaliser of O therefore adds back each key tile's largest-weight
-      // rounding error, so a row's dominant weight divides out exactly.  L keeps
-      // the fp32 sum, which has none of that rounding.
-      const float inv = p.o_scale / (C::kIsFp8 ? l + lc : l);
+      // rounding (relative error up to 2^-4 for e4m3, 2^-9 for bf16) would
+      // scale O by as much; the normaliser of O therefore adds back each key
+      // tile's largest-weight rounding error, so a row's dominant weight divides
+      // out exactly.  L keeps the fp32 sum, which has none of that rounding.
+      const float inv = p.o_scale / (l + lc);
       const float lse_v = (m2 + log2f(l) - C::kPExp) * 0.69314718055994530942f;
       if (row < N) {
         if (p.part_o != nullptr) {

@@ -11,6 +11,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "exp2_poly.h"
+
 namespace attn {
 
 // Status codes mirrored from include/attn_fa2.h (device side).
@@ -278,24 +280,6 @@ __device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]
       : "memory");
 }
 
-// Split-phase load of 128 columns: columns [0, 64) are loaded and waited for,
-// then the load of the next 64 columns is issued and left in flight, so work on
-// the first half overlaps it.  The second half's registers must not be read
-// before tmem_wait_ld_dep(b), which waits for the load and passes b through as
-// read-write operands, so that no use of b can be scheduled above the wait.
-__device__ __forceinline__ void tmem_ld64_then_ld64(uint32_t ta, uint32_t (&a)[64], uint32_t tb, uint32_t (&b)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];"
-      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(a[32]), "=r"(a[33]), "=r"(a[34]), "=r"(a[35]), "=r"(a[36]), "=r"(a[37]), "=r"(a[38]), "=r"(a[39]), "=r"(a[40]), "=r"(a[41]), "=r"(a[42]), "=r"(a[43]), "=r"(a[44]), "=r"(a[45]), "=r"(a[46]), "=r"(a[47]), "=r"(a[48]), "=r"(a[49]), "=r"(a[50]), "=r"(a[51]), "=r"(a[52]), "=r"(a[53]), "=r"(a[54]), "=r"(a[55]), "=r"(a[56]), "=r"(a[57]), "=r"(a[58]), "=r"(a[59]), "=r"(a[60]), "=r"(a[61]), "=r"(a[62]), "=r"(a[63]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31]), "=r"(b[32]), "=r"(b[33]), "=r"(b[34]), "=r"(b[35]), "=r"(b[36]), "=r"(b[37]), "=r"(b[38]), "=r"(b[39]), "=r"(b[40]), "=r"(b[41]), "=r"(b[42]), "=r"(b[43]), "=r"(b[44]), "=r"(b[45]), "=r"(b[46]), "=r"(b[47]), "=r"(b[48]), "=r"(b[49]), "=r"(b[50]), "=r"(b[51]), "=r"(b[52]), "=r"(b[53]), "=r"(b[54]), "=r"(b[55]), "=r"(b[56]), "=r"(b[57]), "=r"(b[58]), "=r"(b[59]), "=r"(b[60]), "=r"(b[61]), "=r"(b[62]), "=r"(b[63])
-      : "r"(ta), "r"(tb)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t (&b)[64]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31]), "+r"(b[32]), "+r"(b[33]), "+r"(b[34]), "+r"(b[35]), "+r"(b[36]), "+r"(b[37]), "+r"(b[38]), "+r"(b[39]), "+r"(b[40]), "+r"(b[41]), "+r"(b[42]), "+r"(b[43]), "+r"(b[44]), "+r"(b[45]), "+r"(b[46]), "+r"(b[47]), "+r"(b[48]), "+r"(b[49]), "+r"(b[50]), "+r"(b[51]), "+r"(b[52]), "+r"(b[53]), "+r"(b[54]), "+r"(b[55]), "+r"(b[56]), "+r"(b[57]), "+r"(b[58]), "+r"(b[59]), "+r"(b[60]), "+r"(b[61]), "+r"(b[62]), "+r"(b[63]) : : "memory");
-}
-
 // Load 32 lanes x 128 columns (32-bit) and wait for completion in the same statement.
 __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -411,6 +395,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x for both lanes of a packed pair by the polynomial of exp2_poly.h, on the
+// FMA pipe: x is raised to kExp2PolyFloor, n = round(x) by the 1.5 * 2^23 add
+// (n lands in the low bits of t), f = x - n in [-1/2, 1/2], p(f) by Horner,
+// and n is added to p's exponent field: bits(p) + bits(t) * 2^23 (the magic's
+// own bits shift out of the 32-bit word).
+__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x2) {
+  const float x0 = fmaxf(f2_lo(x2), kExp2PolyFloor), x1 = fmaxf(f2_hi(x2), kExp2PolyFloor);
+  const uint64_t x = f2_pack(x0, x1);
+  const uint64_t t = f2_add(x, f2_pack(12582912.f, 12582912.f));
+  const uint64_t n = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);
+  uint64_t p = f2_fma(f2_pack(kExp2PolyC3, kExp2PolyC3), f, f2_pack(kExp2PolyC2, kExp2PolyC2));
+  p = f2_fma(p, f, f2_pack(kExp2PolyC1, kExp2PolyC1));
+  p = f2_fma(p, f, f2_pack(kExp2PolyC0, kExp2PolyC0));
+  const uint32_t lo = static_cast<uint32_t>(p) + static_cast<uint32_t>(t) * 8388608u;
+  const uint32_t hi = static_cast<uint32_t>(p >> 32) + static_cast<uint32_t>(t >> 32) * 8388608u;
+  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

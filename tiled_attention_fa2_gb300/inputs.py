@@ -104,6 +104,9 @@ WORKLOADS = {
     "dit_e4m3": dict(B=1, H=56, N=30272, d=128, dtype="e4m3", causal=False, q_mult=1.0),
     "long_causal_bf16": dict(B=1, H=8, N=32768, d=128, dtype="bf16", causal=True, q_mult=1.0),
     "long_causal_e4m3": dict(B=1, H=8, N=32768, d=128, dtype="e4m3", causal=True, q_mult=1.0),
+    # The DiT shape on 16 of its 56 heads: the small case whole-kernel profiles
+    # are taken on (inputs still larger than L2, a quarter of the run time).
+    "dit_e4m3_16h": dict(B=1, H=16, N=30272, d=128, dtype="e4m3", causal=False, q_mult=1.0),
     # Grouped-query attention at the head counts of a Llama-3-70B-class model
     # (64 query heads sharing 8 K/V heads, d = 128), causal prefill of 8192 tokens.
     "prefill_gqa_bf16": dict(B=1, H=64, Hkv=8, N=8192, d=128, dtype="bf16", causal=True, q_mult=1.0),
