@@ -47,6 +47,8 @@ FLUSH_BYTES = 512 << 20
 # Published figures for an exact workload (other hardware: context only).
 PUBLISHED_TFLOPS = {"dit_e4m3": 26.27e12 / 123.6e-3 / 1e12}  # RTX 5080, final FP8 CuTe-DSL kernel
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 datasheet dense (no 2:4 sparsity) tensor peaks, TFLOP/s: context beside the measured ones.
+DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "e4m3": 4500.0}
 
 
 # The sources the tensor-core forward kernel and its launch are built from; a
@@ -70,6 +72,16 @@ def load_peaks():
         with open(p) as f:
             return json.load(f), "measured"
     return FALLBACK_PEAKS, "fallback"
+
+
+def datasheet_fraction(dtype: str, achieved: float) -> dict:
+    """The datasheet dense peak of the contraction dtype and the fraction of it
+    reached (reported beside the measured-peak fraction; fp32 runs on the CUDA
+    cores and has none)."""
+    p = DATASHEET_DENSE_TFLOPS.get(dtype)
+    if p is None:
+        return {}
+    return {"datasheet_peak": p, "frac_of_datasheet": round(achieved / p, 4)}
 
 
 def dtype_peak(dtype: str, peaks: dict):
@@ -353,7 +365,8 @@ def run_gpu_arm(args, w):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peaks_src}: {peak_note}",
-                     "traffic": profile_traffic(args.workload)},
+                     "traffic": profile_traffic(args.workload),
+                     **datasheet_fraction(w["dtype"], achieved)},
         "clocks": clocks,
         "e2e": {"value": round(job_throughput(flops, world, e2e_steps, e2e_ms), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
@@ -599,7 +612,8 @@ def run_gpu_bwd(args, w):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peaks_src}: {peak_note}",
-                     "note": "whole step (three launches) against the tensor peak", "traffic": None},
+                     "note": "whole step (three launches) against the tensor peak", "traffic": None,
+                     **datasheet_fraction("bf16", achieved)},
         "clocks": clocks,
         "e2e": {"value": round(flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
