@@ -96,8 +96,8 @@ def test_backward_non_default_scale(scale, causal):
 @pytest.mark.parametrize("order", ["key", "head"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_causal_backward_in_either_grid_order(order, d, monkeypatch):
-    # A causal backward grid runs key-tile-major or head-major, chosen from the
-    # shape; ATTN_BWD_GRID_ORDER forces one.  Both match the oracle.
+    # A causal backward deals its items key-tile-major (the default) or
+    # head-major (ATTN_BWD_GRID_ORDER=head).  Both match the oracle.
     monkeypatch.setenv("ATTN_BWD_GRID_ORDER", order)
     got, ref = run_case(2, 3, 513, d, True, seed=31 + d)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
@@ -118,11 +118,11 @@ def _grads(B, H, N, d, causal, seed):
 
 
 def test_long_causal_backward_is_the_same_in_both_grid_orders(monkeypatch):
-    # The long causal shape (B=1, H=8, N=32768, d=128), where the shape rule picks
-    # head-major: each CTA computes the dK, dV rows of its own key tile whatever
-    # the order, so they are bit-identical to the key-tile-major run; dQ differs
-    # only by the order of its fp32 reduce-adds.
-    monkeypatch.setenv("ATTN_BWD_GRID_ORDER", "key")
+    # The long causal shape (B=1, H=8, N=32768, d=128): each work item computes
+    # the dK, dV rows of its own key tile whatever the order, so they are
+    # bit-identical across the orders; dQ differs only by the order of its fp32
+    # reduce-adds.
+    monkeypatch.setenv("ATTN_BWD_GRID_ORDER", "head")
     a = _grads(1, 8, 32768, 128, True, seed=41)
     monkeypatch.delenv("ATTN_BWD_GRID_ORDER")
     b = _grads(1, 8, 32768, 128, True, seed=41)

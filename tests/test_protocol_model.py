@@ -208,85 +208,118 @@ def test_the_model_catches_a_barrier_two_phases_ahead():
         next(wait_phase(c, 0))
 
 
-def run_backward(seed, n_it, slots, double_s):
-    """The backward kernel's CTA (one key tile, n_it query tiles): producer, MMA
-    warp and the eight pass warps, with `slots` Q/dO slots and, when
-    `double_s`, the next query tile's S^T issued into a second buffer during
-    the current pass (the d = 64 layout)."""
+def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
+    """The persistent backward kernel's CTA: producer, MMA warp and the eight pass
+    warps over a list of work items (key tiles), item r having items[r] query
+    tiles, with `slots` Q/dO slots and, when `double_s`, the next query tile's S^T
+    issued into a second buffer during the current pass (the d = 64 layout).
+    Steps are numbered across items (T); per-step barriers take phase T, per-slot
+    ones phase T // slots, per-item ones (kv, fin, acc_free) phase r.  The next
+    item's K/V load waits until the last MMA that reads the current K/V has
+    completed (fin), and its first dV/dK products until the epilogue has read the
+    previous item's dV/dK out of TMEM (acc_free)."""
     rng = random.Random(seed)
     bars = {name: Barrier(name, count) for name, count in (
-        ("kv", 1), ("s_full", 1), ("dq_full", 1), ("drain_done", 8), ("fin", 1), ("p_full0", 8), ("p_full1", 8))}
+        ("kv", 1), ("s_full", 1), ("dq_full", 1), ("drain_done", 8), ("fin", 1), ("acc_free", 8), ("p_full0", 8),
+        ("p_full1", 8))}
     for s in range(slots):
         for name, count in (("q_full", 1), ("q_empty", 1), ("stage_free", 8)):
             bars[f"{name}{s}"] = Barrier(f"{name}{s}", count)
     loads, commits = [], []
+    total = sum(items)
 
     def slot(t):
         return t % slots
 
     def use(t):
-        return t // slots  # phase index of slot(t)'s barriers for query tile t
+        return t // slots  # phase index of slot(t)'s barriers for step t
 
     def wait(name, phase):
         return wait_phase(bars[name], phase)
 
     reduced = []
+    stored = []
+    acc_read = [0] * len(items)  # pass warps that have read item r's dV, dK out of TMEM
 
     def producer():
-        loads.append("kv")
-
-        def finish_tile(t):  # dQ of tile t staged: reduce-add it, then the slot is free
+        def finish_tile(t):  # dQ of step t staged: reduce-add it, then the slot is free
             yield from wait(f"stage_free{slot(t)}", use(t))
             reduced.append(t)
             yield "work"
 
-        for it in range(n_it):
-            if it >= slots:
-                yield from finish_tile(it - slots)
-            loads.append(f"q_full{slot(it)}")
-        for t in range(max(0, n_it - slots), n_it):
+        T = 0
+        for r, n_it in enumerate(items):
+            for it in range(n_it):
+                if T >= slots:
+                    yield from finish_tile(T - slots)
+                loads.append(f"q_full{slot(T)}")
+                if it == 0:
+                    if r > 0:
+                        yield from wait("fin", r - 1)  # the previous item's K/V are no longer read
+                        assert bars["fin"].done >= r, "K/V reloaded while the previous item's MMAs may read them"
+                    loads.append("kv")
+                T += 1
+        for t in range(max(0, total - slots), total):
             yield from finish_tile(t)
 
     def mma():
-        yield from wait("kv", 0)
-        yield from wait("q_full0", 0)
-        commits.append("s_full")
-        for it in range(n_it):
-            s = slot(it)
-            if double_s and it + 1 < n_it:
-                yield from wait(f"q_full{slot(it + 1)}", use(it + 1))
-                if it > 0:
-                    yield from wait("drain_done", it - 1)
-            yield from wait("p_full0", it)
-            yield from wait("p_full1", it)
-            commits.append(f"q_empty{s}")
-            commits.append("dq_full")
-            if it + 1 < n_it:
-                if not double_s:
-                    yield from wait(f"q_full{slot(it + 1)}", use(it + 1))
-                    yield from wait("drain_done", it)
-                commits.append("s_full")
-        commits.append("fin")
-        yield from wait("fin", 0)
+        T = 0
+        for r, n_it in enumerate(items):
+            yield from wait("kv", r)
+            yield from wait(f"q_full{slot(T)}", use(T))
+            if T > 0:
+                yield from wait("drain_done", T - 1)  # S^T columns: the previous step's dQ is out
+            commits.append("s_full")
+            for it in range(n_it):
+                s = slot(T)
+                if double_s and it + 1 < n_it:
+                    yield from wait(f"q_full{slot(T + 1)}", use(T + 1))
+                    if it > 0:
+                        yield from wait("drain_done", T - 1)
+                if it == 0 and r > 0:
+                    if not skip_acc_free_wait:
+                        yield from wait("acc_free", r - 1)  # dV, dK of the previous item read out
+                    # the first dV/dK products of item r overwrite the accumulators
+                    assert acc_read[r - 1] == 8, f"item {r} overwrites dV/dK before item {r - 1} was read"
+                yield from wait("p_full0", T)
+                yield from wait("p_full1", T)
+                commits.append(f"q_empty{s}")
+                commits.append("dq_full")
+                if it + 1 < n_it:
+                    if not double_s:
+                        yield from wait(f"q_full{slot(T + 1)}", use(T + 1))
+                        yield from wait("drain_done", T)
+                    commits.append("s_full")
+                T += 1
+            commits.append("fin")
+        yield from wait("fin", len(items) - 1)
 
-    def pass_warp():
-        for it in range(n_it):
-            s = slot(it)
-            yield from wait("s_full", it)
-            yield from wait(f"q_full{s}", use(it))
+    def pass_warp(w):
+        T = 0
+        for r, n_it in enumerate(items):
+            for it in range(n_it):
+                s = slot(T)
+                yield from wait("s_full", T)
+                yield from wait(f"q_full{s}", use(T))
+                yield "work"
+                bars["p_full0"].arrive()
+                yield "work"
+                bars["p_full1"].arrive()
+                yield from wait("dq_full", T)
+                yield "work"
+                bars["drain_done"].arrive()
+                yield from wait(f"q_empty{s}", use(T))
+                yield "work"
+                bars[f"stage_free{s}"].arrive()
+                T += 1
+            yield from wait("fin", r)
             yield "work"
-            bars["p_full0"].arrive()
-            yield "work"
-            bars["p_full1"].arrive()
-            yield from wait("dq_full", it)
-            yield "work"
-            bars["drain_done"].arrive()
-            yield from wait(f"q_empty{s}", use(it))
-            yield "work"
-            bars[f"stage_free{s}"].arrive()
-        yield from wait("fin", 0)
+            acc_read[r] += 1
+            bars["acc_free"].arrive()
+            if w == 0:
+                stored.append(r)
 
-    roles = [producer(), mma()] + [pass_warp() for _ in range(8)]
+    roles = [producer(), mma()] + [pass_warp(w) for w in range(8)]
     alive = list(range(len(roles)))
     idle = 0
     while alive:
@@ -305,12 +338,19 @@ def run_backward(seed, n_it, slots, double_s):
             continue
         idle = idle + 1 if step == "blocked" else 0
         assert not (idle > 200 * len(alive) and not loads and not commits), f"deadlock, roles {alive} waiting"
-    assert sorted(reduced) == list(range(n_it)), "every query tile's dQ is reduced exactly once"
+    assert sorted(reduced) == list(range(total)), "every step's dQ is reduced exactly once"
+    assert stored == list(range(len(items))), "every item's dK, dV stored once, in order"
     return True
 
 
-@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("items", [[1], [2], [16], [3, 1, 5], [1, 1, 1, 1], [16, 2, 7], [2, 3]])
 @pytest.mark.parametrize("slots,double_s", [(2, False), (3, True)])
-def test_backward_barrier_protocol_has_no_deadlock_or_phase_aliasing(n_it, slots, double_s):
+def test_backward_barrier_protocol_has_no_deadlock_or_phase_aliasing(items, slots, double_s):
     for seed in range(12):
-        assert run_backward(seed, n_it, slots, double_s)
+        assert run_backward(seed, items, slots, double_s)
+
+
+def test_the_backward_model_catches_a_missing_accumulator_hand_off():
+    with pytest.raises(AssertionError, match="overwrites dV/dK"):
+        for seed in range(50):
+            run_backward(seed, [2, 2, 2], 2, False, skip_acc_free_wait=True)

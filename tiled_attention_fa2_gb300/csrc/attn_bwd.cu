@@ -11,7 +11,8 @@
 // softmax:  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,
 // dK = scale dS^T Q.
 //
-// Main kernel, one CTA per (key tile j, b*h), scores held transposed: TMEM lane
+// Main kernel, persistent (one CTA per SM, each walking a snake-ordered list of
+// work items (key tile j, b*h)), scores held transposed: TMEM lane
 // r is key r of the tile, so S^T = K_j Q_i^T and dP^T = V_j dO_i^T put one key
 // row of each per thread, and the P^T and dS^T that thread computes are already
 // the A operands of dV += P^T dO_i and dK += dS^T Q_i, straight from TMEM.
@@ -35,8 +36,12 @@
 // being read by then) stage it, scaled, in that slot as fp32 TMA boxes; the
 // producer warp issues the reduce-adds into the fp32 accumulator and waits for
 // them to read the slot before loading the query tile after next into it, so
-// neither the reduce nor its completion sits on the pass warps' path.  After the
-// last query tile: dK * scale and dV to bf16.
+// neither the reduce nor its completion sits on the pass warps' path.  After an
+// item's last query tile: dK * scale and dV to bf16.  Across items the next item
+// starts under the current one's tail: its first Q, dO load into the slot the
+// finished query tiles freed, its K, V as soon as the last MMA that reads the
+// current ones completes, and its S^T, dP^T while the pass warps drain the last
+// dQ and read dV, dK out; only its first dV/dK products wait for that read-out.
 #include <cstdlib>
 #include <cstring>
 
@@ -71,7 +76,7 @@ struct BwdCfg {
   static constexpr int kBoxes = D / 32;  // dQ staging boxes per query tile
   static constexpr int kL2 = kDS + kPSBytes, kDrow = kL2 + kSlots * 512;
   static constexpr int kBar = kDrow + kSlots * 512;
-  static constexpr int kUsed = kBar + 16 * 8 + 16;
+  static constexpr int kUsed = kBar + 17 * 8 + 16;  // 17 mbarriers, then the TMEM address
   static constexpr int kSmemBytes = (kUsed + 1024 < kMaxSmem) ? kUsed + 1024 : kMaxSmem;
   static_assert(kUsed <= kMaxSmem, "shared memory layout too large");
   // TMEM columns: dV | dK | S^T (then dQ; two buffers when kDblS) | dP^T (then P^T
@@ -351,32 +356,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kBar);
   const uint32_t b0 = smem_u32(bars);
   const uint32_t kv_bar = b0, s_full = b0 + 8, dq_full = b0 + 16, drain_done = b0 + 24, fin_bar = b0 + 32;
+  // dV and dK of the current item read out of TMEM by the epilogue (the next
+  // item's first dV/dK products may overwrite them).
+  const uint32_t acc_free = b0 + 128;
   // P^T / dS^T chunk q (queries [32q, 32q + 32) and [64 + 32q, 96 + 32q)) written
   auto p_full = [&](int q) { return b0 + 40 + 8 * q; };
   auto q_full = [&](int s) { return b0 + 56 + 8 * s; };       // slot loaded
   auto q_empty = [&](int s) { return b0 + 80 + 8 * s; };      // slot's Q, dO read by the MMAs
   auto stage_free = [&](int s) { return b0 + 104 + 8 * s; };  // slot's dQ staged
-  // Query tile t uses slot t % kSlots for the (t / kSlots)-th time.
+  // Steps (one query tile of one work item) are numbered T across the CTA's
+  // items: step T uses slot T % kSlots for the (T / kSlots)-th time, per-step
+  // barriers complete one phase per step, per-item ones (kv_bar, fin_bar,
+  // acc_free) one phase per item.
   constexpr int kSl = C::kSlots;
   auto slot_of = [](int t) { return t % kSl; };
   auto use_par = [](int t) { return static_cast<uint32_t>((t / kSl) & 1); };
-  // S^T (then dQ) columns of query tile t.
+  // S^T (then dQ) columns of step t.
   auto col_s = [](int t) { return C::kColS + (C::kDblS ? 128u * static_cast<uint32_t>(t & 1) : 0u); };
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N, n_kt = (N + 127) >> 7, n_pad = n_kt * 128;
-  const int x = static_cast<int>(blockIdx.x);
-  // Grid order: key-tile-major (all heads' key tile 0, then key tile 1, ...: the
-  // heaviest causal CTAs first) or head-major (one head's key tiles after the
+  // Persistent: work item x = (key tile j, b*h); round r of CTA c takes item
+  // r G + c (even r) or r G + G - 1 - c (odd r), a snake over the item order.
+  // Item order: key-tile-major (all heads' key tile 0, then key tile 1, ...: the
+  // heaviest causal items first) or head-major (one head's key tiles after the
   // other, heaviest first within the head, so the CTAs running together reduce
   // into one head's dQ, which stays in L2).  Non-causal grids are always
   // head-major.
   const bool hm = !kCausal || head_major != 0;
-  const int j = hm ? x % n_kt : x / p.BH, bh = hm ? x / n_kt : x % p.BH;
-  const int n_it = kCausal ? n_kt - j : n_kt;  // causal: query tiles j .. n_kt - 1
-  // Query tile of this CTA's t-th step.
-  auto qtile = [&](int t) { return kCausal || j + t < n_kt ? j + t : j + t - n_kt; };
+  const int total = n_kt * p.BH;
+  auto item_of = [&](int r) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+  };
+  auto key_tile_of = [&](int x) { return hm ? x % n_kt : x / p.BH; };
+  auto head_of = [&](int x) { return hm ? x / n_kt : x % p.BH; };
+  auto steps_of = [&](int j) { return kCausal ? n_kt - j : n_kt; };  // causal: query tiles j .. n_kt - 1
+  // Query tile of the t-th step of an item with key tile j.
+  auto qtile = [&](int j, int t) { return kCausal || j + t < n_kt ? j + t : j + t - n_kt; };
   const uint64_t lim = p.timeout_ns;
 
   if (tid == 0) {
@@ -387,6 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     mbar_init(dq_full, 1);
     mbar_init(drain_done, 8);
     mbar_init(fin_bar, 1);
+    mbar_init(acc_free, 8);
     for (int s = 0; s < kSl; ++s) {
       mbar_init(q_full(s), 1);
       mbar_init(q_empty(s), 1);
@@ -411,224 +430,272 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
 
   if (warp == kProducerWarp) {
     // ============================================================ TMA producer
-    mbar_arrive_expect_tx_elect(kv_bar, 2 * C::kTileBytes);
-    for (int b = 0; b < C::kBlocks; ++b) {
-      tma_load_3d_elect(sK + b * 16384, &p.tm_k, kv_bar, b * 64, j * 128, bh);
-      tma_load_3d_elect(sV + b * 16384, &p.tm_v, kv_bar, b * 64, j * 128, bh);
-    }
-    // dQ of query tile t, staged in its slot by the pass warps: reduce-add the
-    // boxes into the accumulator and wait until they are read, so the slot can
-    // be reloaded.
+    // (b*h, query tile) of the last kSl steps, by slot: where their dQ goes.
+    int ring_bh[kSl], ring_q[kSl];
+    // dQ of step t, staged in its slot by the pass warps: reduce-add the boxes
+    // into the accumulator and wait until they are read, so the slot can be
+    // reloaded.
     auto finish_tile = [&](int t) {
       const int s = slot_of(t);
       if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), use_par(t), p.status, lim, 64))) return false;
       if (lane == 0) {
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, qtile(t) * 128, bh);
+          tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, ring_q[s] * 128, ring_bh[s]);
         bulk_commit_group();
         bulk_wait_read_all();
       }
       __syncwarp();
       return true;
     };
-    int issued = 0;
+    int T = 0, n_items = 0, issued = 0;  // steps done, items and steps whose loads were issued
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = slot_of(it), i = qtile(it);
-      if (it >= kSl) {  // the slot's previous query tile is read and its dQ reduced
-        ok = finish_tile(it - kSl);
-        if (!ok) break;
+    for (int r = 0; ok; ++r) {
+      const int x = item_of(r);
+      if (x >= total) break;
+      const int j = key_tile_of(x), bh = head_of(x), n_it = steps_of(j);
+      for (int it = 0; ok && it < n_it; ++it, ++T) {
+        const int s = slot_of(T), i = qtile(j, it);
+        if (T >= kSl) {  // the slot's previous step is read and its dQ reduced
+          ok = finish_tile(T - kSl);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
+        for (int b = 0; b < C::kBlocks; ++b) {
+          tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
+          tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
+        }
+        const size_t v0 = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
+        bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
+        bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
+        ring_bh[s] = bh;
+        ring_q[s] = i;
+        issued = T + 1;
+        if (it == 0) {
+          // K_j, V_j over the previous item's, once its last MMAs (which read them) are done.
+          if (r > 0) ok = __all_sync(0xffffffffu, mbar_wait(fin_bar, (r - 1) & 1, p.status, lim));
+          if (!ok) break;
+          mbar_arrive_expect_tx_elect(kv_bar, 2 * C::kTileBytes);
+          for (int b = 0; b < C::kBlocks; ++b) {
+            tma_load_3d_elect(sK + b * 16384, &p.tm_k, kv_bar, b * 64, j * 128, bh);
+            tma_load_3d_elect(sV + b * 16384, &p.tm_v, kv_bar, b * 64, j * 128, bh);
+          }
+          ++n_items;
+        }
       }
-      mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
-      for (int b = 0; b < C::kBlocks; ++b) {
-        tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
-        tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
-      }
-      const size_t v0 = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
-      bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
-      bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
-      issued = it + 1;
     }
-    for (int t = n_it >= kSl ? n_it - kSl : 0; ok && t < n_it; ++t) ok = finish_tile(t);
+    for (int t = T >= kSl ? T - kSl : 0; ok && t < T; ++t) ok = finish_tile(t);
     if (lane == 0) bulk_wait_all();  // the dQ reduce-adds have completed
     // Copies still in flight (only after a failed wait elsewhere) land before exit.
-    mbar_wait(kv_bar, 0, p.status, lim);
-    for (int it = issued > kSl ? issued - kSl : 0; it < issued; ++it)
-      mbar_wait(q_full(slot_of(it)), use_par(it), p.status, lim);
+    if (n_items > 0) mbar_wait(kv_bar, (n_items - 1) & 1, p.status, lim);
+    for (int t = issued > kSl ? issued - kSl : 0; t < issued; ++t)
+      mbar_wait(q_full(slot_of(t)), use_par(t), p.status, lim);
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
-    bool ok = mbar_wait(kv_bar, 0, p.status, lim) && mbar_wait(q_full(0), 0, p.status, lim);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    int T = 0, n_fin = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int x = item_of(r);
+      if (x >= total) break;
+      const int n_it = steps_of(key_tile_of(x));
+      // The item's K_j, V_j and first Q, dO; its first S^T goes over the
+      // previous step's dQ columns, once they are drained.
+      ok = mbar_wait(kv_bar, r & 1, p.status, lim) && mbar_wait(q_full(slot_of(T)), use_par(T), p.status, lim) &&
+           (T == 0 || mbar_wait(drain_done, (T - 1) & 1, p.status, lim));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       tc_fence_after();
-      mma_rows<D>(tmem + col_s(0), sK, sQ(0));
-      mma_rows<D>(tmem + C::kColDP, sV, sDO(0));
+      mma_rows<D>(tmem + col_s(T), sK, sQ(slot_of(T)));
+      mma_rows<D>(tmem + C::kColDP, sV, sDO(slot_of(T)));
       mma_commit_elect(s_full);
-    }
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = slot_of(it);
-      if (C::kDblS && it + 1 < n_it) {
-        // The next query tile's S^T into the other buffer, to run during this
-        // pass, once that buffer's dQ (query tile it - 1) is out of TMEM.
-        const int s1 = slot_of(it + 1);
-        ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(it + 1), p.status, lim) &&
-                                         (it == 0 || mbar_wait(drain_done, (it - 1) & 1, p.status, lim)));
+      for (int it = 0; ok && it < n_it; ++it, ++T) {
+        const int s = slot_of(T);
+        if (C::kDblS && it + 1 < n_it) {
+          // The next step's S^T into the other buffer, to run during this pass,
+          // once that buffer's dQ (step T - 1) is out of TMEM.
+          const int s1 = slot_of(T + 1);
+          ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(T + 1), p.status, lim) &&
+                                           (it == 0 || mbar_wait(drain_done, (T - 1) & 1, p.status, lim)));
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows<D>(tmem + col_s(T + 1), sK, sQ(s1));
+        }
+        if (it == 0 && r > 0) {
+          // The first dV/dK products of the item overwrite the accumulators:
+          // the previous item's epilogue must have read them.
+          ok = __all_sync(0xffffffffu, mbar_wait(acc_free, (r - 1) & 1, p.status, lim));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dV and dK over the queries of the first P^T / dS^T chunks while the pass
+        // computes the second ones.
+        ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), T & 1, p.status, lim));
         if (!ok) break;
         tc_fence_after();
-        mma_rows<D>(tmem + col_s(it + 1), sK, sQ(s1));
-      }
-      // dV and dK over the queries of the first P^T / dS^T chunks while the pass
-      // computes the second ones.
-      ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), it & 1, p.status, lim));
-      if (!ok) break;
-      tc_fence_after();
-      mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(it), sDO(s), 0, it > 0);
-      mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(it) + 8, sQ(s), 0, it > 0);
-      ok = __all_sync(0xffffffffu, mbar_wait(p_full(1), it & 1, p.status, lim));
-      if (!ok) break;
-      tc_fence_after();
-      mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(it), sDO(s), 1, true);
-      mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(it) + 8, sQ(s), 1, true);
-      mma_commit_elect(q_empty(s));
-      mma_dq<D>(tmem + col_s(it), sDS, sK);
-      mma_commit_elect(dq_full);
-      if (it + 1 < n_it) {
-        const int s1 = slot_of(it + 1);
-        if (!C::kDblS) {
-          ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(it + 1), p.status, lim));
-          if (!ok) break;
-          tc_fence_after();
+        mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(T), sDO(s), 0, it > 0);
+        mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(T) + 8, sQ(s), 0, it > 0);
+        ok = __all_sync(0xffffffffu, mbar_wait(p_full(1), T & 1, p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(T), sDO(s), 1, true);
+        mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(T) + 8, sQ(s), 1, true);
+        mma_commit_elect(q_empty(s));
+        mma_dq<D>(tmem + col_s(T), sDS, sK);
+        mma_commit_elect(dq_full);
+        if (it + 1 < n_it) {
+          const int s1 = slot_of(T + 1);
+          if (!C::kDblS) {
+            ok = __all_sync(0xffffffffu, mbar_wait(q_full(s1), use_par(T + 1), p.status, lim));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));  // the pass has read dP^T
+          if (!C::kDblS) {
+            ok = __all_sync(0xffffffffu, mbar_wait(drain_done, T & 1, p.status, lim));
+            if (!ok) break;
+            tc_fence_after();
+            mma_rows<D>(tmem + col_s(T + 1), sK, sQ(s1));
+          }
+          mma_commit_elect(s_full);
         }
-        mma_rows<D>(tmem + C::kColDP, sV, sDO(s1));  // the pass has read dP^T
-        if (!C::kDblS) {
-          ok = __all_sync(0xffffffffu, mbar_wait(drain_done, it & 1, p.status, lim));
-          if (!ok) break;
-          tc_fence_after();
-          mma_rows<D>(tmem + col_s(it + 1), sK, sQ(s1));
-        }
-        mma_commit_elect(s_full);
       }
+      if (!ok) break;
+      // dV, dK of the item complete (the epilogue may read them) and K_j, V_j
+      // are no longer read (the producer may load the next item's).
+      mma_commit_elect(fin_bar);
+      ++n_fin;
     }
-    // Every MMA of this CTA completes before the epilogue reads dV, dK (and
-    // before TMEM is freed).
-    mma_commit_elect(fin_bar);
-    mbar_wait(fin_bar, 0, p.status, lim);
+    // Every MMA of this CTA completes before TMEM is freed.
+    if (!ok) {
+      mma_commit_elect(fin_bar);
+      ++n_fin;
+    }
+    if (n_fin > 0) mbar_wait(fin_bar, (n_fin - 1) & 1, p.status, lim);
   } else {
     // ============================================================ pass / drain warps
     const int qd = warp & 3, g = warp >> 2;
     const int key_local = qd * 32 + lane;       // this thread's key row (TMEM lane)
-    const int key = j * 128 + key_local;
-    const bool key_ok = key < N;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = slot_of(it), i = qtile(it);
-      ok = pass_all(mbar_wait(s_full, it & 1, p.status, lim) && mbar_wait(q_full(s), use_par(it), p.status, lim));
-      if (!ok) break;
-      tc_fence_after();
-      const bool diag = kCausal && i == j;
-      const bool mask = diag || !key_ok;
-      // Four 16-query groups (queries 64g + 16u ..): group u + 1's S^T and dP^T
-      // loads are in flight while group u is computed; P^T and dS^T go over the
-      // group's own S^T columns.  After groups 1 and 3 (a 32-query chunk) the
-      // stores are waited for and the chunk is handed to the MMA warp.
-      uint32_t sv[2][16], dpv[2][16];
-      tmem_ld16x2_issue(tmem + lane_base + col_s(it) + 64 * g, sv[0], tmem + lane_base + C::kColDP + 64 * g, dpv[0]);
-      tmem_wait_ld16x2(sv[0], dpv[0]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int b = u & 1;
-        const int col0 = 64 * g + 16 * u;  // first query (tile-local) of this group
-        if (u < 3)
-          tmem_ld16x2_issue(tmem + lane_base + col_s(it) + col0 + 16, sv[b ^ 1],
-                            tmem + lane_base + C::kColDP + col0 + 16, dpv[b ^ 1]);
-        uint32_t pw[8], dw[8];
-        if (mask)
-          pass_sub16<true>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
-                           pw, dw);
-        else
-          pass_sub16<false>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
-                            pw, dw);
-        tmem_st8x2_issue(tmem + lane_base + col_s(it) + col0, pw, tmem + lane_base + col_s(it) + col0 + 8, dw);
-        st_shared_v4(sw128_chunk(sDS, key_local, col0 >> 3), dw[0], dw[1], dw[2], dw[3]);
-        st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + 1), dw[4], dw[5], dw[6], dw[7]);
-        if (u & 1) {
-          // P^T and dS^T of this chunk in TMEM are read by dV and dK; dS^T in
-          // shared memory (async proxy) by dQ after the last chunk.
-          tmem_wait_st();
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(p_full(u >> 1));
+    int T = 0;
+    for (int r = 0; ok; ++r) {
+      const int x = item_of(r);
+      if (x >= total) break;
+      const int j = key_tile_of(x), bh = head_of(x), n_it = steps_of(j);
+      const int key = j * 128 + key_local;
+      const bool key_ok = key < N;
+      for (int it = 0; ok && it < n_it; ++it, ++T) {
+        const int s = slot_of(T), i = qtile(j, it);
+        ok = pass_all(mbar_wait(s_full, T & 1, p.status, lim) && mbar_wait(q_full(s), use_par(T), p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        const bool diag = kCausal && i == j;
+        const bool mask = diag || !key_ok;
+        // Four 16-query groups (queries 64g + 16u ..): group u + 1's S^T and dP^T
+        // loads are in flight while group u is computed; P^T and dS^T go over the
+        // group's own S^T columns.  After groups 1 and 3 (a 32-query chunk) the
+        // stores are waited for and the chunk is handed to the MMA warp.
+        uint32_t sv[2][16], dpv[2][16];
+        tmem_ld16x2_issue(tmem + lane_base + col_s(T) + 64 * g, sv[0], tmem + lane_base + C::kColDP + 64 * g, dpv[0]);
+        tmem_wait_ld16x2(sv[0], dpv[0]);
+  #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int b = u & 1;
+          const int col0 = 64 * g + 16 * u;  // first query (tile-local) of this group
+          if (u < 3)
+            tmem_ld16x2_issue(tmem + lane_base + col_s(T) + col0 + 16, sv[b ^ 1],
+                              tmem + lane_base + C::kColDP + col0 + 16, dpv[b ^ 1]);
+          uint32_t pw[8], dw[8];
+          if (mask)
+            pass_sub16<true>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
+                             pw, dw);
+          else
+            pass_sub16<false>(sv[b], dpv[b], sL2(s) + 4 * col0, sDr(s) + 4 * col0, sl2x2, key_local, col0, key_ok, diag,
+                              pw, dw);
+          tmem_st8x2_issue(tmem + lane_base + col_s(T) + col0, pw, tmem + lane_base + col_s(T) + col0 + 8, dw);
+          st_shared_v4(sw128_chunk(sDS, key_local, col0 >> 3), dw[0], dw[1], dw[2], dw[3]);
+          st_shared_v4(sw128_chunk(sDS, key_local, (col0 >> 3) + 1), dw[4], dw[5], dw[6], dw[7]);
+          if (u & 1) {
+            // P^T and dS^T of this chunk in TMEM are read by dV and dK; dS^T in
+            // shared memory (async proxy) by dQ after the last chunk.
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(u >> 1));
+          }
+          if (u < 3) tmem_wait_ld16x2(sv[b ^ 1], dpv[b ^ 1]);
         }
-        if (u < 3) tmem_wait_ld16x2(sv[b ^ 1], dpv[b ^ 1]);
+
+        // ---- drain dQ_i = dS K_j (S^T columns).  Warp w holds query rows 32 (w % 4)..
+        // and columns [g d/2, (g+1) d/2).  First out of TMEM (the next S^T may then
+        // be issued over it), then staged in this query tile's slot once its Q and
+        // dO are read; the producer warp reduce-adds the staged boxes.
+        ok = pass_all(mbar_wait(dq_full, T & 1, p.status, lim));
+        if (!ok) break;
+        tc_fence_after();
+        const int row_local = key_local;  // TMEM lane = query row of dQ_i
+        uint32_t gq[D / 2];
+  #pragma unroll
+        for (int c = 0; c < D / 2; c += 32)
+          tmem_ld32_sync(tmem + lane_base + col_s(T) + g * (D / 2) + c, *reinterpret_cast<uint32_t(*)[32]>(gq + c));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(drain_done);
+        // Staging address of this thread's 16-byte chunk q4 of box b (row row_local).
+        const uint32_t stg = sSlot(s);
+        auto chunk_addr = [&](uint32_t slot_base, int b, int q4) {
+          return slot_base + b * 16384 + row_local * 128 + ((q4 ^ (row_local & 7)) << 4);
+        };
+        // The slot's Q and dO have been read (dV and dK were issued before dQ_i).
+        ok = pass_all(mbar_wait(q_empty(s), use_par(T), p.status, lim));
+        if (!ok) break;
+  #pragma unroll
+        for (int c = 0; c < D / 2; c += 32)
+  #pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            st_shared_v4(chunk_addr(stg, (g * (D / 2) + c) / 32, q4),
+                         __float_as_uint(__uint_as_float(gq[c + 4 * q4]) * p.scale),
+                         __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 1]) * p.scale),
+                         __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 2]) * p.scale),
+                         __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 3]) * p.scale));
+        fence_proxy_async_smem();  // read by the producer's TMA reduce-adds
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stage_free(s));
       }
 
-      // ---- drain dQ_i = dS K_j (S^T columns).  Warp w holds query rows 32 (w % 4)..
-      // and columns [g d/2, (g+1) d/2).  First out of TMEM (the next S^T may then
-      // be issued over it), then staged in this query tile's slot once its Q and
-      // dO are read; the producer warp reduce-adds the staged boxes.
-      ok = pass_all(mbar_wait(dq_full, it & 1, p.status, lim));
-      if (!ok) break;
-      tc_fence_after();
-      const int row_local = key_local;  // TMEM lane = query row of dQ_i
-      uint32_t gq[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32)
-        tmem_ld32_sync(tmem + lane_base + col_s(it) + g * (D / 2) + c, *reinterpret_cast<uint32_t(*)[32]>(gq + c));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(drain_done);
-      // Staging address of this thread's 16-byte chunk q4 of box b (row row_local).
-      const uint32_t stg = sSlot(s);
-      auto chunk_addr = [&](uint32_t slot_base, int b, int q4) {
-        return slot_base + b * 16384 + row_local * 128 + ((q4 ^ (row_local & 7)) << 4);
-      };
-      // The slot's Q and dO have been read (dV and dK were issued before dQ_i).
-      ok = pass_all(mbar_wait(q_empty(s), use_par(it), p.status, lim));
-      if (!ok) break;
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32)
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          st_shared_v4(chunk_addr(stg, (g * (D / 2) + c) / 32, q4),
-                       __float_as_uint(__uint_as_float(gq[c + 4 * q4]) * p.scale),
-                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 1]) * p.scale),
-                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 2]) * p.scale),
-                       __float_as_uint(__uint_as_float(gq[c + 4 * q4 + 3]) * p.scale));
-      fence_proxy_async_smem();  // read by the producer's TMA reduce-adds
-      __syncwarp();
-      if (lane == 0) mbar_arrive(stage_free(s));
-    }
-
-    // ---- epilogue: dK * scale and dV to bf16.  Warp-collective TMEM loads by
-    // every lane; only key rows < N are stored.
-    ok = pass_all(ok && mbar_wait(fin_bar, 0, p.status, lim));
-    if (ok) {
-      tc_fence_after();
-      const size_t kr = static_cast<size_t>(bh) * N + (key_ok ? key : 0);
-      __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
-      __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
-#pragma unroll 1
-      for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
-        uint32_t a[32], b[32];
-        tmem_ld32x2_sync(tmem + lane_base + C::kColDV + c0, a, tmem + lane_base + C::kColDK + c0, b);
-        if (!key_ok) continue;
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 va, vb;
-          va.x = pack_bf16x2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-          va.y = pack_bf16x2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-          va.z = pack_bf16x2(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
-          va.w = pack_bf16x2(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
-          vb.x = pack_bf16x2(__uint_as_float(b[e]) * p.scale, __uint_as_float(b[e + 1]) * p.scale);
-          vb.y = pack_bf16x2(__uint_as_float(b[e + 2]) * p.scale, __uint_as_float(b[e + 3]) * p.scale);
-          vb.z = pack_bf16x2(__uint_as_float(b[e + 4]) * p.scale, __uint_as_float(b[e + 5]) * p.scale);
-          vb.w = pack_bf16x2(__uint_as_float(b[e + 6]) * p.scale, __uint_as_float(b[e + 7]) * p.scale);
-          *reinterpret_cast<uint4*>(dvp + c0 + e) = va;
-          *reinterpret_cast<uint4*>(dkp + c0 + e) = vb;
+      // ---- epilogue of the item: dK * scale and dV to bf16.  Warp-collective
+      // TMEM loads by every lane; only key rows < N are stored.  Once this warp's
+      // loads are done, the next item's first dV/dK products may overwrite them.
+      ok = pass_all(ok && mbar_wait(fin_bar, r & 1, p.status, lim));
+      if (ok) {
+        tc_fence_after();
+        const size_t kr = static_cast<size_t>(bh) * N + (key_ok ? key : 0);
+        __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
+        __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+  #pragma unroll 1
+        for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 32) {
+          uint32_t a[32], b[32];
+          tmem_ld32x2_sync(tmem + lane_base + C::kColDV + c0, a, tmem + lane_base + C::kColDK + c0, b);
+          if (!key_ok) continue;
+  #pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 va, vb;
+            va.x = pack_bf16x2(__uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+            va.y = pack_bf16x2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+            va.z = pack_bf16x2(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+            va.w = pack_bf16x2(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+            vb.x = pack_bf16x2(__uint_as_float(b[e]) * p.scale, __uint_as_float(b[e + 1]) * p.scale);
+            vb.y = pack_bf16x2(__uint_as_float(b[e + 2]) * p.scale, __uint_as_float(b[e + 3]) * p.scale);
+            vb.z = pack_bf16x2(__uint_as_float(b[e + 4]) * p.scale, __uint_as_float(b[e + 5]) * p.scale);
+            vb.w = pack_bf16x2(__uint_as_float(b[e + 6]) * p.scale, __uint_as_float(b[e + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(dvp + c0 + e) = va;
+            *reinterpret_cast<uint4*>(dkp + c0 + e) = vb;
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_free);
       }
     }
   }
@@ -642,26 +709,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
   }
 }
 
-// Grid order of a causal backward.  Key-tile-major puts the heaviest CTAs
-// (key tile 0 sees every query tile) first across all heads, which balances the
-// SMs best, but the CTAs running together then reduce into every head's dQ at
-// once.  Head-major keeps one head's dQ in L2 at the cost of a coarser balance.
-// It is chosen when the fp32 dQ accumulator exceeds half of L2 and the heaviest
-// CTA (n_kt query tiles) is at most a fifth of an SM's share of the grid's work
-// (BH n_kt (n_kt + 1) / 2 query tiles over the SMs), i.e. 10 SMs <= BH (n_kt + 1).
-// ATTN_BWD_GRID_ORDER=key or =head in the environment overrides the choice.
-cudaError_t causal_head_major(const BwdParams& p, int d, int* out) {
+// Item order of a causal backward.  Key-tile-major puts the heaviest items
+// (key tile 0 sees every query tile) first across all heads, and the snake that
+// deals the items to the persistent CTAs then evens out their work.  Head-major
+// keeps one head's dQ accumulator in L2, but with the static snake its uneven
+// item weights balance badly (long causal shape: 1034 against 1202 TFLOP/s for
+// key-tile-major), so key-tile-major is the default and
+// ATTN_BWD_GRID_ORDER=head (or =key) in the environment chooses explicitly.
+cudaError_t causal_head_major(int* out) {
   const char* env = std::getenv("ATTN_BWD_GRID_ORDER");
-  if (env && std::strcmp(env, "head") == 0) return *out = 1, cudaSuccess;
-  if (env && std::strcmp(env, "key") == 0) return *out = 0, cudaSuccess;
-  int dev = 0, sms = 0, l2 = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-  if (e != cudaSuccess) return e;
-  const long long n_kt = (p.N + 127) / 128;
-  const long long acc_bytes = static_cast<long long>(p.BH) * p.N * d * 4;
-  *out = (2 * acc_bytes > l2 && 10LL * sms <= static_cast<long long>(p.BH) * (n_kt + 1)) ? 1 : 0;
+  *out = (env && std::strcmp(env, "head") == 0) ? 1 : 0;
   return cudaSuccess;
 }
 
@@ -672,9 +729,14 @@ cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = smem_opt_in_once(kern, BwdCfg<D>::kSmemBytes, opted_in);
   if (e != cudaSuccess) return e;
   int head_major = 1;
-  if (kCausal && (e = causal_head_major(p, D, &head_major)) != cudaSuccess) return e;
+  if (kCausal && (e = causal_head_major(&head_major)) != cudaSuccess) return e;
   const long long n_kt = (p.N + 127) / 128;
-  kern<<<static_cast<unsigned>(n_kt * p.BH), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p, head_major);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long items = n_kt * p.BH;
+  const long long grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
+  kern<<<static_cast<unsigned>(grid), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p, head_major);
   return cudaGetLastError();
 }
 
