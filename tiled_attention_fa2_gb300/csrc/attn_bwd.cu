@@ -53,6 +53,20 @@
 namespace attn {
 namespace {
 
+// Optional event trace (compile with -DATTN_TRACE): cycle stamps of the first
+// 64 steps of CTA 0, for timeline analysis.
+#ifdef ATTN_TRACE
+__device__ unsigned long long g_bwd_trace[64 * 16];
+#define BWD_TRACE(cond, step, ev)                                                        \
+  do {                                                                                   \
+    if ((cond) && blockIdx.x == 0 && (step) < 64) g_bwd_trace[(step) * 16 + (ev)] = clock64(); \
+  } while (0)
+#else
+#define BWD_TRACE(cond, step, ev) \
+  do {                            \
+  } while (0)
+#endif
+
 constexpr int kBwdThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kPSBytes = 128 * 128 * 2;  // one [128 key][128 query] bf16 tile (dS^T)
@@ -507,6 +521,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       mma_rows<D>(tmem + col_s(T), sK, sQ(slot_of(T)));
       mma_rows<D>(tmem + C::kColDP, sV, sDO(slot_of(T)));
       mma_commit_elect(s_full);
+      BWD_TRACE(lane == 0, T, 0);
       for (int it = 0; ok && it < n_it; ++it, ++T) {
         const int s = slot_of(T);
         if (C::kDblS && it + 1 < n_it) {
@@ -530,17 +545,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         // computes the second ones.
         ok = __all_sync(0xffffffffu, mbar_wait(p_full(0), T & 1, p.status, lim));
         if (!ok) break;
+        BWD_TRACE(lane == 0, T, 1);
         tc_fence_after();
         mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(T), sDO(s), 0, it > 0);
         mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(T) + 8, sQ(s), 0, it > 0);
         ok = __all_sync(0xffffffffu, mbar_wait(p_full(1), T & 1, p.status, lim));
         if (!ok) break;
+        BWD_TRACE(lane == 0, T, 2);
         tc_fence_after();
         mma_ts_half<D>(tmem + C::kColDV, tmem + col_s(T), sDO(s), 1, true);
         mma_ts_half<D>(tmem + C::kColDK, tmem + col_s(T) + 8, sQ(s), 1, true);
         mma_commit_elect(q_empty(s));
         mma_dq<D>(tmem + col_s(T), sDS, sK);
         mma_commit_elect(dq_full);
+        BWD_TRACE(lane == 0, T, 3);
         if (it + 1 < n_it) {
           const int s1 = slot_of(T + 1);
           if (!C::kDblS) {
@@ -552,10 +570,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
           if (!C::kDblS) {
             ok = __all_sync(0xffffffffu, mbar_wait(drain_done, T & 1, p.status, lim));
             if (!ok) break;
+            BWD_TRACE(lane == 0, T, 4);
             tc_fence_after();
             mma_rows<D>(tmem + col_s(T + 1), sK, sQ(s1));
           }
           mma_commit_elect(s_full);
+          BWD_TRACE(lane == 0, T + 1, 0);
         }
       }
       if (!ok) break;
@@ -588,6 +608,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         const int s = slot_of(T), i = qtile(j, it);
         ok = pass_all(mbar_wait(s_full, T & 1, p.status, lim) && mbar_wait(q_full(s), use_par(T), p.status, lim));
         if (!ok) break;
+        BWD_TRACE(tid == 0, T, 8);
         tc_fence_after();
         const bool diag = kCausal && i == j;
         const bool mask = diag || !key_ok;
@@ -623,6 +644,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(u >> 1));
+            BWD_TRACE(tid == 0, T, 9 + (u >> 1));
           }
           if (u < 3) tmem_wait_ld16x2(sv[b ^ 1], dpv[b ^ 1]);
         }
@@ -633,6 +655,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         // dO are read; the producer warp reduce-adds the staged boxes.
         ok = pass_all(mbar_wait(dq_full, T & 1, p.status, lim));
         if (!ok) break;
+        BWD_TRACE(tid == 0, T, 11);
         tc_fence_after();
         const int row_local = key_local;  // TMEM lane = query row of dQ_i
         uint32_t gq[D / 2];
@@ -642,6 +665,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(drain_done);
+        BWD_TRACE(tid == 0, T, 12);
         // Staging address of this thread's 16-byte chunk q4 of box b (row row_local).
         const uint32_t stg = sSlot(s);
         auto chunk_addr = [&](uint32_t slot_base, int b, int q4) {
@@ -662,6 +686,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         fence_proxy_async_smem();  // read by the producer's TMA reduce-adds
         __syncwarp();
         if (lane == 0) mbar_arrive(stage_free(s));
+        BWD_TRACE(tid == 0, T, 13);
       }
 
       // ---- epilogue of the item: dK * scale and dV to bf16.  Warp-collective
@@ -741,6 +766,13 @@ cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#ifdef ATTN_TRACE
+// Trace builds only: read the stamps of the last backward launch.
+extern "C" int attn_trace_bwd(unsigned long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_bwd_trace, sizeof(g_bwd_trace)));
+}
+#endif
 
 cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stream) {
   if (d != 64 && d != 128) return cudaErrorInvalidValue;
