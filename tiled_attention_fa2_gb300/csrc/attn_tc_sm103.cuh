@@ -126,8 +126,6 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   }
 }
 
-// Exponentials of keys [64h, 64h + 64) of this thread's score row, in place,
-// and their packed row sums.
 // Exponentials of one packed pair of exponents (log2 units), in place into
 // s[c], s[c + 1]: the exponential unit, or (pairs the split-exponential option
 // selects) the polynomial on the FMA pipe.  Pair k of a 64-key half is
