@@ -97,29 +97,75 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   else tmem_st32_sync(taddr, r);
 }
 
+// A group of SS-form MMAs (kind::f16 or kind::f8f6f4) from one elected lane:
+// slice kk uses descriptors a0 + da[kk], b0 + da[kk]; the first accumulates
+// only if `acc0`, the others always.
+template <bool kFp8, int kN>
+__device__ __forceinline__ void mma_ss_group(uint32_t d, uint64_t a0, uint64_t b0, const uint32_t (&da)[kN],
+                                             uint32_t idesc, uint32_t acc0) {
+  uint64_t a[kN], b[kN];
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    a[i] = a0 + da[i];
+    b[i] = b0 + da[i];
+  }
+  if constexpr (kN == 4) {
+    if constexpr (kFp8)
+      asm volatile(
+          "{\n .reg .pred p, e;\n setp.ne.b32 p, %10, 0;\n elect.sync _|e, 0xffffffff;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %9, p;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %9, 1;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %6, %9, 1;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %8, %9, 1;\n}" ::"r"(d),
+          "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]), "r"(idesc),
+          "r"(acc0)
+          : "memory");
+    else
+      asm volatile(
+          "{\n .reg .pred p, e;\n setp.ne.b32 p, %10, 0;\n elect.sync _|e, 0xffffffff;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %9, p;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %9, 1;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %9, 1;\n"
+          " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %9, 1;\n}" ::"r"(d),
+          "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]), "r"(idesc),
+          "r"(acc0)
+          : "memory");
+  } else {
+    static_assert(kN % 4 == 0, "groups of four");
+#pragma unroll
+    for (int g = 0; g < kN; g += 4) {
+      const uint32_t sub[4] = {da[g] - da[g], da[g + 1] - da[g], da[g + 2] - da[g], da[g + 3] - da[g]};
+      mma_ss_group<kFp8, 4>(d, a0 + da[g], b0 + da[g], sub, idesc, g == 0 ? acc0 : 1u);
+    }
+  }
+}
+
 template <class C>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_base, uint32_t k_base) {
+  // Descriptors of the first K slice; slice kk starts `off` bytes further on,
+  // which adds off / 16 to the start-address field (shared addresses stay
+  // below 2^18, so the 14-bit field never carries).
+  uint32_t da[C::kQkSteps];
 #pragma unroll
   for (int kk = 0; kk < C::kQkSteps; ++kk) {
     const uint32_t byte = kk * C::kMmaK * C::kElem;                 // offset inside a row
-    const uint32_t off = (byte / 128) * C::kBlockBytes + (byte % 128);
-    const uint64_t a = sdesc_sw128(q_base + off, 16, 1024);
-    const uint64_t b = sdesc_sw128(k_base + off, 16, 1024);
-    if constexpr (C::kIsFp8) mma_f8_ss_elect(tmem_s, a, b, C::kIdescQK, kk > 0);
-    else mma_f16_ss_elect(tmem_s, a, b, C::kIdescQK, kk > 0);
+    da[kk] = ((byte / 128) * C::kBlockBytes + (byte % 128)) >> 4;
   }
+  mma_ss_group<C::kIsFp8, C::kQkSteps>(tmem_s, sdesc_sw128(q_base, 16, 1024), sdesc_sw128(k_base, 16, 1024), da,
+                                       C::kIdescQK, 0u);
 }
 
 // One half (keys [64h, 64h + 64)) of O += P V.
 template <class C, int kHalf>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base, bool accumulate) {
   constexpr int kSteps = C::kPvSteps / 2;
+  // V slot: key rows of 128 bytes per column block; the B operand is MN-major
+  // (d contiguous): SBO = 8 key rows, LBO = next 128-byte column block.
+  const uint64_t b0 = sdesc_sw128(v_base, C::kBlockBytes, 1024);
 #pragma unroll
   for (int i = 0; i < kSteps; ++i) {
     const int kk = kHalf * kSteps + i;
-    // V slot: key rows of 128 bytes per column block; the B operand is MN-major
-    // (d contiguous): SBO = 8 key rows, LBO = next 128-byte column block.
-    const uint64_t b = sdesc_sw128(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 1024);
+    const uint64_t b = b0 + ((kk * C::kMmaK * 128) >> 4);
     const uint32_t a = tmem_p + kk * 8;  // kMmaK elements of P = 8 TMEM columns
     if constexpr (C::kIsFp8) mma_f8_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
     else mma_f16_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
