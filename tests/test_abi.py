@@ -173,3 +173,35 @@ def test_backward_workspace_size(lib):
         assert binding.bwd_workspace_size(B, H, N, d) == want
     with pytest.raises(binding.AttnError):
         binding.bwd_workspace_size(1, 1, 16, 96)
+
+
+def call_gqa(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=8, Hkv=2, N=256, d=128, scale=0.1, qd=1.0, kd=1.0,
+             vd=1.0, causal=0, dtype=1)
+    a.update(kw)
+    return lib.attn_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["N"], a["d"],
+                            a["scale"], a["qd"], a["kd"], a["vd"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hkv=0), 1), (dict(Hkv=3), 1), (dict(Hkv=16), 1), (dict(H=0), 1), (dict(Hkv=-2), 1),
+    (dict(q=None), 1), (dict(dtype=2, kd=0.0), 1), (dict(dtype=2, vd=float("nan")), 1), (dict(d=96), 2),
+    (dict(k=FAKE + 8), 3), (dict(causal=2), 1),
+])
+def test_gqa_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
+    assert call_gqa(lib, **kw) == status
+    assert lib.attn_last_error() != b""
+
+
+def test_gqa_descales_are_ignored_for_bf16(lib):
+    # Only an ATTN_E4M3 call reads the descales; a bf16 call with zero descales
+    # passes validation and fails only on the (deliberately) unsupported d.
+    assert call_gqa(lib, dtype=1, qd=0.0, kd=0.0, vd=0.0, d=96) == 2
+
+
+def test_poly_exp2_setter_round_trips(lib):
+    prev = lib.attn_set_poly_exp2(1)
+    assert prev in (0, 1)
+    assert lib.attn_set_poly_exp2(0) == 1
+    assert lib.attn_set_poly_exp2(7) == -1  # refused, nothing changed
+    assert lib.attn_set_poly_exp2(prev) == 0

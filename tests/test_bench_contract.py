@@ -96,3 +96,41 @@ def test_gpu_count_must_match_the_launch():
     r = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"), "--gpus", "2",
                         "--impl", "reference"], capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 2 and "WORLD_SIZE=1" in r.stderr
+
+
+def test_datasheet_fraction_beside_the_measured_one():
+    assert bench.datasheet_fraction("bf16", 1125.0) == {"datasheet_peak": 2250.0, "frac_of_datasheet": 0.5}
+    assert bench.datasheet_fraction("e4m3", 2250.0) == {"datasheet_peak": 4500.0, "frac_of_datasheet": 0.5}
+    assert bench.datasheet_fraction("f32", 1.0) == {}
+
+
+def test_grouped_query_workloads_read_their_own_kv_heads():
+    w = inputs.WORKLOADS["prefill_gqa_bf16"]
+    assert bench.kv_heads(w) == 8 and w["H"] % bench.kv_heads(w) == 0
+    assert bench.kv_heads(inputs.WORKLOADS["dit_e4m3"]) == 56
+
+
+def test_oracle_head_inputs_follow_the_head_map():
+    # query head h of batch b reads K/V head b * H_kv + h // (H / H_kv)
+    import numpy as np
+    import oracle
+
+    w = dict(B=2, H=4, Hkv=2, N=8, d=4, dtype="f32", causal=False, q_mult=1.0)
+    host, ds = bench.make_host_inputs(w)
+    assert tuple(host[1].shape) == (2, 2, 8, 4)
+    for h in range(8):
+        q, k, v = bench._oracle_head_inputs(w, host, ds, h)
+        b, hq = divmod(h, 4)
+        g = oracle.kv_head_of(hq, 4, 2)
+        assert np.array_equal(q, host[0][b, hq].double().numpy())
+        assert np.array_equal(k, host[1][b, g].double().numpy())
+        assert np.array_equal(v, host[2][b, g].double().numpy())
+
+
+def test_backward_pass_refuses_grouped_query_workloads():
+    import subprocess
+    import sys
+
+    r = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"), "--pass", "bwd",
+                        "--workload", "prefill_gqa_bf16"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "multi-head attention only" in r.stderr
