@@ -57,9 +57,10 @@ struct TcCfg {
   static constexpr int kPCols = kFp8 ? 32 : 64;              // TMEM columns of one P tile
   // Conditional rescale ("Kernels and Memory in LLM Inference", FlashAttention-4
   // section, item 2): the reference max used in the exponentials moves only
-  // when the row max grows by more than kTau (log2 units), so p <= 2^kTau.
-  // P is stored as p * 2^kPExp; for e4m3 2^(kTau + kPExp) = 256 <= 448 (max
-  // finite).  A stale reference leaves a row's dominant weight at 2^x, x in
+  // when the row max grows by more than kTau (log2 units), so p <= 2^kTau:
+  // 8 doublings for bf16 (the section's figure); e4m3 stores P as p * 2^kPExp
+  // and keeps 2^(kTau + kPExp) = 256 <= 448 (its largest finite value) with a
+  // bound of 4, so that small weights keep their e4m3 precision.  A stale reference leaves a row's dominant weight at 2^x, x in
   // (0, kTau], which the P format rounds while l sums the unrounded p; the
   // normaliser of O adds that rounding back (top_weight_rounding), so the drift
   // costs no accuracy.
