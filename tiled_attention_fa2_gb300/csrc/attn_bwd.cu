@@ -452,12 +452,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
     auto finish_tile = [&](int t) {
       const int s = slot_of(t);
       if (!__all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), use_par(t), p.status, lim, 64))) return false;
+      BWD_TRACE(lane == 0, t, 14);
       if (lane == 0) {
         for (int b = 0; b < C::kBoxes; ++b)
           tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, ring_q[s] * 128, ring_bh[s]);
         bulk_commit_group();
         bulk_wait_read_all();
       }
+      BWD_TRACE(lane == 0, t, 15);
       __syncwarp();
       return true;
     };
@@ -473,6 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
           ok = finish_tile(T - kSl);
           if (!ok) break;
         }
+        BWD_TRACE(lane == 0, T, 6);
         mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
         for (int b = 0; b < C::kBlocks; ++b) {
           tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
