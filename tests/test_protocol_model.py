@@ -106,6 +106,7 @@ def run(seed, causal, BH, N, G, stages):
     def mma():
         it = nq = 0
         npv = [0, 0]
+        early_v = stages <= 5  # shallow ring: V_j's slot released before the next S, K_{j+1} only tested early
         for k0, k1 in items:
             yield from wait("q_full0", nq)
             yield from wait(f"slot_full{it % stages}", it // stages)
@@ -122,7 +123,16 @@ def run(seed, causal, BH, N, G, stages):
                 sv = it % stages
                 yield from wait(f"slot_full{sv}", it // stages)
                 itk = it + 1
+                k_bar = f"slot_full{itk % stages}"
+                # K_{j+1} before the P waits: a deep ring waits for it there, a
+                # shallow one takes it there only if it has landed already
                 k_ready = False
+                if j + 1 < k1:
+                    if early_v:
+                        k_ready = bars[k_bar].done == itk // stages + 1
+                    else:
+                        yield from wait(k_bar, itk // stages)
+                        k_ready = True
                 for t in (0, 1):
                     kv_end = k1 if t else k0
                     if j < kv_end:
@@ -130,18 +140,22 @@ def run(seed, causal, BH, N, G, stages):
                             yield from wait(f"o_empty{t}", nq - 1)
                         yield from wait(f"p_lo{t}", npv[t])
                         yield from wait(f"p_hi{t}", npv[t])
+                        if t == 1 and early_v:
+                            commit(f"slot_empty{sv}")
+                        if j + 1 < kv_end:
+                            if not k_ready:
+                                yield from wait(k_bar, itk // stages)
+                                k_ready = True
+                            commit(f"s_full{t}")
+                            if j + 2 == kv_end:
+                                commit(f"q_empty{t}")
                         npv[t] += 1
                         if j == kv_end - 1:
                             commit(f"o_full{t}")
-                    if t == 1:
+                        if t == 1 and not early_v:
+                            commit(f"slot_empty{sv}")
+                    elif t == 1:
                         commit(f"slot_empty{sv}")
-                    if j + 1 < kv_end:
-                        if not k_ready:
-                            yield from wait(f"slot_full{itk % stages}", itk // stages)
-                            k_ready = True
-                        commit(f"s_full{t}")
-                        if j + 2 == kv_end:
-                            commit(f"q_empty{t}")
                 if j + 1 < k1:
                     commit(f"slot_empty{itk % stages}")
                 it += 2 if j + 1 < k1 else 1

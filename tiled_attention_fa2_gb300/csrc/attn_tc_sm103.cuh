@@ -98,6 +98,13 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   else tmem_st32_sync(taddr, r);
 }
 
+// A shared-memory descriptor advanced by `off` (bytes / 16) in its start
+// address field.  Shared addresses stay below 2^18, so the 14-bit field never
+// carries: a 32-bit add on the low word suffices.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t d, uint32_t off) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + off);
+}
+
 // A group of SS-form MMAs (kind::f16 or kind::f8f6f4) from one elected lane:
 // slice kk uses descriptors a0 + da[kk], b0 + da[kk]; the first accumulates
 // only if `acc0`, the others always.
@@ -107,8 +114,8 @@ __device__ __forceinline__ void mma_ss_group(uint32_t d, uint64_t a0, uint64_t b
   uint64_t a[kN], b[kN];
 #pragma unroll
   for (int i = 0; i < kN; ++i) {
-    a[i] = a0 + da[i];
-    b[i] = b0 + da[i];
+    a[i] = desc_plus(a0, da[i]);
+    b[i] = desc_plus(b0, da[i]);
   }
   if constexpr (kN == 4) {
     if constexpr (kFp8)
@@ -136,41 +143,85 @@ __device__ __forceinline__ void mma_ss_group(uint32_t d, uint64_t a0, uint64_t b
 #pragma unroll
     for (int g = 0; g < kN; g += 4) {
       const uint32_t sub[4] = {da[g] - da[g], da[g + 1] - da[g], da[g + 2] - da[g], da[g + 3] - da[g]};
-      mma_ss_group<kFp8, 4>(d, a0 + da[g], b0 + da[g], sub, idesc, g == 0 ? acc0 : 1u);
+      mma_ss_group<kFp8, 4>(d, desc_plus(a0, da[g]), desc_plus(b0, da[g]), sub, idesc, g == 0 ? acc0 : 1u);
     }
   }
 }
 
+// Shared-memory descriptors of a Q or K tile (K-major, 128-byte swizzle) and
+// of a V tile (the B operand of P V, MN-major: d contiguous, SBO = 8 key rows,
+// LBO = the next 128-byte column block).
 template <class C>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_base, uint32_t k_base) {
-  // Descriptors of the first K slice; slice kk starts `off` bytes further on,
-  // which adds off / 16 to the start-address field (shared addresses stay
-  // below 2^18, so the 14-bit field never carries).
+__device__ __forceinline__ uint64_t qk_desc(uint32_t tile) { return sdesc_sw128(tile, 16, 1024); }
+template <class C>
+__device__ __forceinline__ uint64_t v_desc(uint32_t tile) { return sdesc_sw128(tile, C::kBlockBytes, 1024); }
+
+// S = Q K^T from the tiles' descriptors (qk_desc); slice kk of the
+// contraction starts `off` bytes further on, which adds off / 16 to the
+// start-address field.
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t qd, uint64_t kd) {
   uint32_t da[C::kQkSteps];
 #pragma unroll
   for (int kk = 0; kk < C::kQkSteps; ++kk) {
     const uint32_t byte = kk * C::kMmaK * C::kElem;                 // offset inside a row
     da[kk] = ((byte / 128) * C::kBlockBytes + (byte % 128)) >> 4;
   }
-  mma_ss_group<C::kIsFp8, C::kQkSteps>(tmem_s, sdesc_sw128(q_base, 16, 1024), sdesc_sw128(k_base, 16, 1024), da,
-                                       C::kIdescQK, 0u);
+  mma_ss_group<C::kIsFp8, C::kQkSteps>(tmem_s, qd, kd, da, C::kIdescQK, 0u);
 }
 
-// One half (keys [64h, 64h + 64)) of O += P V.
+// A group of TS-form MMAs (A from TMEM) from one elected lane, in one
+// statement: MMA i reads A at TMEM address a[i] and B by descriptor b[i]; the
+// first accumulates only if `acc0`, the others always.
+#define ATTN_TS_MMA(kind, ia, ib, acc) " @e tcgen05.mma.cta_group::1.kind::" kind " [%0], [%" ia "], %" ib ", %1, " acc ";\n"
+template <bool kFp8, int kN>
+__device__ __forceinline__ void mma_ts_group(uint32_t d, const uint32_t (&a)[kN], const uint64_t (&b)[kN],
+                                             uint32_t idesc, uint32_t acc0) {
+  static_assert(kN == 2 || kN == 4, "groups of two or four");
+  if constexpr (kN == 2) {
+    if constexpr (kFp8)
+      asm volatile("{\n .reg .pred p, e;\n setp.ne.b32 p, %2, 0;\n elect.sync _|e, 0xffffffff;\n" ATTN_TS_MMA(
+                       "f8f6f4", "3", "5", "p") ATTN_TS_MMA("f8f6f4", "4", "6", "1") "}" ::"r"(d),
+                   "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
+                   : "memory");
+    else
+      asm volatile("{\n .reg .pred p, e;\n setp.ne.b32 p, %2, 0;\n elect.sync _|e, 0xffffffff;\n" ATTN_TS_MMA(
+                       "f16", "3", "5", "p") ATTN_TS_MMA("f16", "4", "6", "1") "}" ::"r"(d),
+                   "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
+                   : "memory");
+  } else {
+    if constexpr (kFp8)
+      asm volatile("{\n .reg .pred p, e;\n setp.ne.b32 p, %2, 0;\n elect.sync _|e, 0xffffffff;\n" ATTN_TS_MMA(
+                       "f8f6f4", "3", "7", "p") ATTN_TS_MMA("f8f6f4", "4", "8", "1")
+                       ATTN_TS_MMA("f8f6f4", "5", "9", "1") ATTN_TS_MMA("f8f6f4", "6", "10", "1") "}" ::"r"(d),
+                   "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]),
+                   "l"(b[2]), "l"(b[3])
+                   : "memory");
+    else
+      asm volatile("{\n .reg .pred p, e;\n setp.ne.b32 p, %2, 0;\n elect.sync _|e, 0xffffffff;\n" ATTN_TS_MMA(
+                       "f16", "3", "7", "p") ATTN_TS_MMA("f16", "4", "8", "1") ATTN_TS_MMA("f16", "5", "9", "1")
+                       ATTN_TS_MMA("f16", "6", "10", "1") "}" ::"r"(d),
+                   "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]),
+                   "l"(b[2]), "l"(b[3])
+                   : "memory");
+  }
+}
+#undef ATTN_TS_MMA
+
+// One half (keys [64h, 64h + 64)) of O += P V, V given by its descriptor
+// (v_desc), issued as one group.
 template <class C, int kHalf>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t vd, bool accumulate) {
   constexpr int kSteps = C::kPvSteps / 2;
-  // V slot: key rows of 128 bytes per column block; the B operand is MN-major
-  // (d contiguous): SBO = 8 key rows, LBO = next 128-byte column block.
-  const uint64_t b0 = sdesc_sw128(v_base, C::kBlockBytes, 1024);
+  uint32_t a[kSteps];
+  uint64_t b[kSteps];
 #pragma unroll
   for (int i = 0; i < kSteps; ++i) {
     const int kk = kHalf * kSteps + i;
-    const uint64_t b = b0 + ((kk * C::kMmaK * 128) >> 4);
-    const uint32_t a = tmem_p + kk * 8;  // kMmaK elements of P = 8 TMEM columns
-    if constexpr (C::kIsFp8) mma_f8_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
-    else mma_f16_ts_elect(tmem_o, a, b, C::kIdescPV, accumulate || i > 0);
+    b[i] = desc_plus(vd, (kk * C::kMmaK * 128) >> 4);
+    a[i] = tmem_p + kk * 8;  // kMmaK elements of P = 8 TMEM columns
   }
+  mma_ts_group<C::kIsFp8, kSteps>(tmem_o, a, b, C::kIdescPV, accumulate ? 1u : 0u);
 }
 
 // Exponentials of one packed pair of exponents (log2 units), in place into
@@ -461,6 +512,8 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
       };
       int it = 0, nq = 0;
       int np[2] = {0, 0};  // P tiles consumed per query tile (phase of p_lo / p_hi)
+      const uint64_t qd0 = qk_desc<C>(q_base), qd1 = qk_desc<C>(q_base + C::kTileBytes);
+      constexpr bool kShallowRing = C::kStages <= 5;
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int item = item_of_round(r);
@@ -471,14 +524,14 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
         if (!ok) break;
         tc_fence_after();
         {
-          const uint32_t kb = slot_base + (it % kS) * C::kTileBytes;
-          issue_qk<C>(tmem + 0, q_base, kb);
+          const uint64_t kd = qk_desc<C>(slot_base + (it % kS) * C::kTileBytes);
+          issue_qk<C>(tmem + 0, qd0, kd);
           mma_commit_elect(s_full(0));
           if (w.kv_end0 == 1) mma_commit_elect(q_empty(0));  // the item's last use of Q_0
           ok = wait_all(q_full(1), nq & 1);
           if (!ok) break;
           tc_fence_after();
-          issue_qk<C>(tmem + 128, q_base + C::kTileBytes, kb);
+          issue_qk<C>(tmem + 128, qd1, kd);
           mma_commit_elect(s_full(1));
           if (w.kv_end1 == 1) mma_commit_elect(q_empty(1));
           mma_commit_elect(slot_empty(it % kS));
@@ -493,8 +546,26 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
           const int itk = it + 1;
           const int sk = itk % kS;
           const bool next = (j + 1 < w.kv_end1);
+          // Descriptors and K_{j+1} (loaded right after V_j) ahead of the P
+          // waits, so that only the MMA issue itself stands between the
+          // softmax's last P store and the next S.  A shallow ring (five 32 KB
+          // slots) can still have K_{j+1} in flight here: it is only tested,
+          // and waited for after P V if it has not landed.
+          const uint64_t vd = v_desc<C>(slot_base + sv * C::kTileBytes);
+          uint64_t kd = 0;
           bool k_ready = false;
-          const uint32_t v_addr = slot_base + sv * C::kTileBytes;
+          if (next) {
+            if constexpr (kShallowRing) {
+              k_ready = __all_sync(0xffffffffu, mbar_test(slot_full(sk), (itk / kS) & 1));
+              if (k_ready) tc_fence_after();
+            } else {
+              ok = wait_all(slot_full(sk), (itk / kS) & 1);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            kd = qk_desc<C>(slot_base + sk * C::kTileBytes);
+          }
+          (void)k_ready;
           for (int t = 0; t < 2 && ok; ++t) {
             const int kv_end = t ? w.kv_end1 : w.kv_end0;
             if (j < kv_end) {
@@ -508,31 +579,41 @@ __global__ void __launch_bounds__(C::kThreads, 1) attn_fwd_tc_kernel(const __gri
               if (!ok) break;
               ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 0);
               tc_fence_after();
-              issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, j > 0);
+              issue_pv<C, 0>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, vd, j > 0);
               ok = wait_all(p_hi(t), np[t] & 1);
               if (!ok) break;
               ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 1);
               tc_fence_after();
-              issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, v_addr, true);
+              issue_pv<C, 1>(tmem + C::kOCol0 + t * C::D, tmem + t * 128, vd, true);
+              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 2);
+              // V_j's last reader: with a shallow ring its slot is released
+              // before the next S is issued, otherwise after it.
+              if constexpr (kShallowRing) {
+                if (t == 1) mma_commit_elect(slot_empty(sv));
+              }
+              if (j + 1 < kv_end) {
+                if constexpr (kShallowRing) {
+                  if (!k_ready) {
+                    ok = wait_all(slot_full(sk), (itk / kS) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    k_ready = true;
+                  }
+                }
+                issue_qk<C>(tmem + t * 128, t ? qd1 : qd0, kd);
+                mma_commit_elect(s_full(t));
+                if (j + 2 == kv_end) mma_commit_elect(q_empty(t));  // the item's last S_t = Q_t K^T
+                ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
+              }
               ++np[t];
               // O_t is read only after its last P.V of the item; earlier rescales
               // rely on S_{j+1} completing after P_j V_j instead.
               if (j == kv_end - 1) mma_commit_elect(o_full(t));
-              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 2);
+            } else if constexpr (kShallowRing) {
+              if (t == 1) mma_commit_elect(slot_empty(sv));
             }
-            if (t == 1) mma_commit_elect(slot_empty(sv));
-            if (j + 1 < kv_end) {
-              if (!k_ready) {
-                ok = wait_all(slot_full(sk), (itk / kS) & 1);
-                if (!ok) break;
-                ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 5);
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk<C>(tmem + t * 128, q_base + t * C::kTileBytes, slot_base + sk * C::kTileBytes);
-              mma_commit_elect(s_full(t));
-              if (j + 2 == kv_end) mma_commit_elect(q_empty(t));  // the item's last S_t = Q_t K^T
-              ATTN_TRACE_EV(tr && lane == 0 && nq == 0, 2 + t, j, 3);
+            if constexpr (!kShallowRing) {
+              if (t == 1) mma_commit_elect(slot_empty(sv));
             }
           }
           if (!ok) break;
