@@ -99,43 +99,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapCacheEntry {
   const void* base;
   CUtensorMapDataType dt;
-  int elem_bytes, BH, N, d;
+  int elem_bytes, BH, N, d, box_rows;
   CUtensorMap map;
 };
 constexpr int kMapCacheSize = 8;
 thread_local MapCacheEntry g_map_cache[kMapCacheSize];
 thread_local int g_map_cache_used = 0, g_map_cache_next = 0;
 
-int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d);
+int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d,
+               int box_rows);
 
-// 3-D map over a [BH, N, d] tensor: dims (d, N, BH), 128-row boxes of one
-// 128-byte column block, 128-byte swizzle, zero fill outside [0, N).
-// Encoded once per distinct argument set (per thread), then reused.
-int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d) {
+// 3-D map over a [BH, N, d] tensor: dims (d, N, BH), boxes of `box_rows` rows
+// (128 by default) of one 128-byte column block, 128-byte swizzle, zero fill
+// outside [0, N) on loads (stores are clipped there).  Encoded once per
+// distinct argument set (per thread), then reused.
+int make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d,
+             int box_rows = 128) {
   for (int i = 0; i < g_map_cache_used; ++i) {
     const MapCacheEntry& e = g_map_cache[i];
-    if (e.base == base && e.dt == dt && e.elem_bytes == elem_bytes && e.BH == BH && e.N == N && e.d == d) {
+    if (e.base == base && e.dt == dt && e.elem_bytes == elem_bytes && e.BH == BH && e.N == N && e.d == d &&
+        e.box_rows == box_rows) {
       *map = e.map;
       return ATTN_OK;
     }
   }
-  const int st = encode_map(map, base, dt, elem_bytes, BH, N, d);
+  const int st = encode_map(map, base, dt, elem_bytes, BH, N, d, box_rows);
   if (st != ATTN_OK) return st;
   MapCacheEntry& e = g_map_cache[g_map_cache_next];
-  e = MapCacheEntry{base, dt, elem_bytes, BH, N, d, *map};
+  e = MapCacheEntry{base, dt, elem_bytes, BH, N, d, box_rows, *map};
   g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
   if (g_map_cache_used < kMapCacheSize) ++g_map_cache_used;
   return ATTN_OK;
 }
 
-int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d) {
+int encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d,
+               int box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
                                  static_cast<cuuint64_t>(N) * d * elem_bytes};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -508,6 +513,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if ((st = make_map(&p.tm_dqacc, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<int>(BH), N, d)) !=
       ATTN_OK)
     return st;
+  // dV and dK leave the kernel as TMA stores of 32-row boxes (one per pass warp).
+  if ((st = make_map(&p.tm_dv, dv, dt, 2, static_cast<int>(BH), N, d, 32)) != ATTN_OK) return st;
+  if ((st = make_map(&p.tm_dk, dk, dt, 2, static_cast<int>(BH), N, d, 32)) != ATTN_OK) return st;
   if ((st = status_ptr(&p.status)) != ATTN_OK) return st;
   const size_t rows = static_cast<size_t>(BH) * N;
   const size_t prows = static_cast<size_t>(BH) * ((static_cast<size_t>(N) + 127) / 128 * 128);

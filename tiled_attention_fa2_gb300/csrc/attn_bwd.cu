@@ -115,6 +115,13 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Bulk tensor store shared -> global (box from the map; rows outside the
+// tensor are not written), tracked like the reduce-adds.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The source shared memory of every committed group has been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -696,8 +703,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       // TMEM loads by every lane; only key rows < N are stored.  Once this warp's
       // loads are done, the next item's first dV/dK products may overwrite them.
       ok = pass_all(ok && mbar_wait(fin_bar, r & 1, p.status, lim));
-      if (ok) {
-        tc_fence_after();
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (D == 128) {
+        // Staged through this warp's 4 KB of the dS^T buffer (the item's last
+        // reader of it, the last dQ product, has completed; the same warp
+        // writes that part again in its next pass): its 32 key rows x 64
+        // columns of dV, then of dK * scale, as 128-byte rows in the 128-byte
+        // swizzle, each written by one TMA store (rows >= N are clipped).
+        const uint32_t stg = sDS + warp * 4096;
+  #pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+          const float f = m ? p.scale : 1.f;
+  #pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t a[32];
+            tmem_ld32_sync(tmem + lane_base + (m ? C::kColDK : C::kColDV) + 64 * g + c0, a);
+  #pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              const int c = (c0 + e) >> 3;  // 16-byte chunk of the 128-byte row
+              st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4),
+                           pack_bf16x2(__uint_as_float(a[e]) * f, __uint_as_float(a[e + 1]) * f),
+                           pack_bf16x2(__uint_as_float(a[e + 2]) * f, __uint_as_float(a[e + 3]) * f),
+                           pack_bf16x2(__uint_as_float(a[e + 4]) * f, __uint_as_float(a[e + 5]) * f),
+                           pack_bf16x2(__uint_as_float(a[e + 6]) * f, __uint_as_float(a[e + 7]) * f));
+            }
+          }
+          if (m == 1) {  // every TMEM read of this warp is done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(m ? &p.tm_dk : &p.tm_dv, stg, 64 * g, j * 128 + 32 * qd, bh);
+            bulk_commit_group();
+            bulk_wait_read_all();  // the staging is reused (dK, then the next pass's dS^T)
+          }
+          __syncwarp();
+        }
+      } else {
         const size_t kr = static_cast<size_t>(bh) * N + (key_ok ? key : 0);
         __nv_bfloat16* dvp = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
         __nv_bfloat16* dkp = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
@@ -726,6 +772,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
         if (lane == 0) mbar_arrive(acc_free);
       }
     }
+    if (lane == 0) bulk_wait_all();  // this warp's dV / dK stores have landed
   }
 
   // ---- teardown: every role has finished with TMEM

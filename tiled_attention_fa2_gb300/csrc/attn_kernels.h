@@ -93,6 +93,8 @@ struct BwdParams {
   CUtensorMap tm_v;
   CUtensorMap tm_do;
   CUtensorMap tm_dqacc; // fp32 [BH, N, d] dQ accumulator (TMA reduce-add target)
+  CUtensorMap tm_dv;    // bf16 [BH, N, d] dV, 32-row boxes (TMA store target)
+  CUtensorMap tm_dk;    // bf16 [BH, N, d] dK, 32-row boxes
   const void* o;        // bf16 [BH, N, d] (forward output)
   const void* dout;     // bf16 [BH, N, d] (upstream gradient dO)
   const float* lse;     // fp32 [BH, N], natural log (forward's L)
