@@ -308,11 +308,13 @@ __device__ __forceinline__ void pass_sub16(const uint32_t (&s)[16], const uint32
         f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, f2_pack(nl.z, nl.w));
     float e[4] = {ex2_approx(f2_lo(x01)), ex2_approx(f2_hi(x01)), ex2_approx(f2_lo(x23)), ex2_approx(f2_hi(x23))};
     if (kMask) {
+      // The group's query columns this key keeps start at `thr` (keys past N
+      // keep none; on the causal diagonal a key keeps the queries at or after
+      // it).  A compound per-element predicate for the same test ran about 3.5
+      // times slower.
+      const int thr = !key_ok ? 32 : (diag ? key_local - q_local0 : -32);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool keep = key_ok && (!diag || key_local <= q_local0 + c + u);
-        e[u] = keep ? e[u] : 0.f;
-      }
+      for (int u = 0; u < 4; ++u) e[u] = (c + u >= thr) ? e[u] : 0.f;
     }
     const uint64_t g01 = f2_add(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2_pack(nd.x, nd.y));
     const uint64_t g23 = f2_add(f2_pack(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2_pack(nd.z, nd.w));
@@ -704,6 +706,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       // loads are done, the next item's first dV/dK products may overwrite them.
       ok = pass_all(ok && mbar_wait(fin_bar, r & 1, p.status, lim));
       if (!ok) break;
+      BWD_TRACE(tid == 0, T - 1, 5);
       tc_fence_after();
       if constexpr (D == 128) {
         // Staged through this warp's 4 KB of the dS^T buffer (the item's last
@@ -733,6 +736,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free);
+            BWD_TRACE(tid == 0, T - 1, 7);
           }
           fence_proxy_async_smem();
           __syncwarp();
