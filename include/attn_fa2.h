@@ -130,7 +130,13 @@ int attn_fwd_split_plan(int B, int H, int N, int d, int n_splits, int* splits_ou
  * (fp32) and its L into `workspace`, then a merge kernel writes o (bf16) and
  * lse (fp32) exactly as attn_fwd would.
  *   dtype     : ATTN_BF16 (descales ignored) or ATTN_E4M3 (per-tensor descales).
- *   causal    : must be 0 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   causal    : must be 0 (ATTN_ERR_UNSUPPORTED otherwise).  Splitting keys is
+ *               for grids smaller than the GPU, i.e. few long query rows such
+ *               as decode, where a query sees every key; under a causal mask a
+ *               query tile's keys end at its diagonal, so equal key ranges
+ *               would leave most ranges of early tiles empty, and causal
+ *               shapes large enough to need it already give the persistent
+ *               kernel (heaviest tiles first) enough work items.
  *   workspace : device, 256-byte aligned, >= the planned bytes, owned by the
  *               caller; its contents are scratch (overwritten by every call).
  * With one resolved range it runs attn_fwd's kernel and touches no workspace.
