@@ -231,7 +231,14 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
     ones phase T // slots, per-item ones (kv, fin, acc_free) phase r.  The next
     item's K/V load waits until the last MMA that reads the current K/V has
     completed (fin), and its first dV/dK products until the epilogue has read the
-    previous item's dV/dK out of TMEM (acc_free)."""
+    previous item's dV/dK out of TMEM (acc_free).  The dS^T shared buffer is
+    written by every pass (each warp its own part) and, at d = 128, by each
+    item's epilogue, which stages dV and dK there for their stores; every
+    step's dQ product reads all of it.  The model checks that no write lands
+    while a dQ product that reads the buffer may still be running (for the
+    epilogue the last step's drain, which waits for that step's dQ, already
+    ensures it), and that no dQ product is issued while a warp is still
+    staging its epilogue there."""
     rng = random.Random(seed)
     bars = {name: Barrier(name, count) for name, count in (
         ("kv", 1), ("s_full", 1), ("dq_full", 1), ("drain_done", 8), ("fin", 1), ("acc_free", 8), ("p_full0", 8),
@@ -254,6 +261,8 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
     reduced = []
     stored = []
     acc_read = [0] * len(items)  # pass warps that have read item r's dV, dK out of TMEM
+    dq_done = [0]                # dQ products completed (the dq_full commit follows each one)
+    epi_done = [0] * 8           # items whose epilogue staging each pass warp has finished
 
     def producer():
         def finish_tile(t):  # dQ of step t staged: reduce-add it, then the slot is free
@@ -298,6 +307,8 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
                 yield from wait("p_full0", T)
                 yield from wait("p_full1", T)
                 commits.append(f"q_empty{s}")
+                # dQ = dS K reads the whole dS^T buffer: no warp may still be staging an epilogue in it
+                assert all(e == r for e in epi_done), f"dQ of step {T} issued during an epilogue's staging"
                 commits.append("dq_full")
                 if it + 1 < n_it:
                     if not double_s:
@@ -315,6 +326,8 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
                 s = slot(T)
                 yield from wait("s_full", T)
                 yield from wait(f"q_full{s}", use(T))
+                # this pass writes its part of dS^T: every earlier dQ product has read the buffer
+                assert dq_done[0] >= T, f"dS^T of step {T} written while an earlier dQ may read it"
                 yield "work"
                 bars["p_full0"].arrive()
                 yield "work"
@@ -327,9 +340,13 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
                 bars[f"stage_free{s}"].arrive()
                 T += 1
             yield from wait("fin", r)
+            # the epilogue stages dV, dK in this warp's part of dS^T: the item's dQ products are done
+            assert dq_done[0] >= T, f"item {r}'s epilogue staged while its last dQ may read dS^T"
             yield "work"
             acc_read[r] += 1
             bars["acc_free"].arrive()
+            yield "work"  # the stores have read the staging
+            epi_done[w] += 1
             if w == 0:
                 stored.append(r)
 
@@ -341,7 +358,10 @@ def run_backward(seed, items, slots, double_s, skip_acc_free_wait=False):
             bars[loads.pop(rng.randrange(len(loads)))].arrive()
             idle = 0
         if commits and rng.random() < 0.3:
-            bars[commits.pop(0)].arrive()
+            c = commits.pop(0)
+            if c == "dq_full":
+                dq_done[0] += 1
+            bars[c].arrive()
             idle = 0
         r = rng.choice(alive)
         try:
