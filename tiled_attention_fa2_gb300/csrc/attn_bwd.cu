@@ -125,6 +125,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The source shared memory of every committed group has been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The source shared memory of every committed group but the most recent one has been read.
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Every committed group has completed (its global writes are done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -480,19 +484,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
       const int j = key_tile_of(x), bh = head_of(x), n_it = steps_of(j);
       for (int it = 0; ok && it < n_it; ++it, ++T) {
         const int s = slot_of(T), i = qtile(j, it);
-        if (T >= kSl) {  // the slot's previous step is read and its dQ reduced
-          ok = finish_tile(T - kSl);
-          if (!ok) break;
-        }
-        BWD_TRACE(lane == 0, T, 6);
-        mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
-        for (int b = 0; b < C::kBlocks; ++b) {
-          tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
-          tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
-        }
         const size_t v0 = static_cast<size_t>(bh) * n_pad + static_cast<size_t>(i) * 128;
-        bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
-        bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
+        if (!C::kDblS && T >= kSl) {
+          // The slot holds step T - 2's staged dQ: reduce-add its dO half first
+          // (own bulk group), and once that half is read load dO and the row
+          // vectors there, their bytes added to the slot's phase without
+          // arriving; the Q load and the phase's one arrival follow when the
+          // rest is read.  Half of the reload overlaps the reduce's reads.
+          const int t0 = T - kSl;
+          ok = __all_sync(0xffffffffu, mbar_wait_sleep(stage_free(s), use_par(t0), p.status, lim, 64));
+          if (!ok) break;
+          BWD_TRACE(lane == 0, t0, 14);
+          if (lane == 0) {
+            for (int b = C::kBoxes / 2; b < C::kBoxes; ++b)  // boxes over the dO half of the slot
+              tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, ring_q[s] * 128, ring_bh[s]);
+            bulk_commit_group();
+            for (int b = 0; b < C::kBoxes / 2; ++b)
+              tma_reduce_add_3d(&p.tm_dqacc, sSlot(s) + b * 16384, 32 * b, ring_q[s] * 128, ring_bh[s]);
+            bulk_commit_group();
+            bulk_wait_read_all_but_last();
+          }
+          __syncwarp();
+          BWD_TRACE(lane == 0, T, 6);
+          mbar_expect_tx_elect(q_full(s), C::kTileBytes + 1024);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
+          bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
+          bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          BWD_TRACE(lane == 0, t0, 15);
+          mbar_arrive_expect_tx_elect(q_full(s), C::kTileBytes);
+          for (int b = 0; b < C::kBlocks; ++b)
+            tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
+        } else {
+          if (T >= kSl) {  // the slot's previous step is read and its dQ reduced
+            ok = finish_tile(T - kSl);
+            if (!ok) break;
+          }
+          BWD_TRACE(lane == 0, T, 6);
+          mbar_arrive_expect_tx_elect(q_full(s), 2 * C::kTileBytes + 1024);
+          for (int b = 0; b < C::kBlocks; ++b) {
+            tma_load_3d_elect(sQ(s) + b * 16384, &p.tm_q, q_full(s), b * 64, i * 128, bh);
+            tma_load_3d_elect(sDO(s) + b * 16384, &p.tm_do, q_full(s), b * 64, i * 128, bh);
+          }
+          bulk_load_elect(sL2(s), p.lse2 + v0, 512, q_full(s));
+          bulk_load_elect(sDr(s), p.drow + v0, 512, q_full(s));
+        }
         ring_bh[s] = bh;
         ring_q[s] = i;
         issued = T + 1;
