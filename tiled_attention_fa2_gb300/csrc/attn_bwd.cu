@@ -125,6 +125,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The source shared memory of every committed group has been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Adds `bytes` to the transactions the barrier's current phase waits for,
+// without arriving (elected lane).
+__device__ __forceinline__ void mbar_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
 // The source shared memory of every committed group but the most recent one has been read.
 __device__ __forceinline__ void bulk_wait_read_all_but_last() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");

@@ -214,15 +214,6 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
       : "memory");
 }
-// Adds `bytes` to the transactions the barrier's current phase waits for,
-// without arriving (elected lane).
-__device__ __forceinline__ void mbar_expect_tx_elect(uint32_t bar, uint32_t bytes) {
-  asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-      " @e mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n}" ::"r"(bar),
-      "r"(bytes)
-      : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
   asm volatile(
       "{\n .reg .pred e;\n .reg .b64 st;\n elect.sync _|e, 0xffffffff;\n"
