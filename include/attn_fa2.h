@@ -53,7 +53,7 @@ typedef enum {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null pointer, size < 1, non-finite or non-positive scale, bad flag */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for (e.g. d = 96 for bf16)  */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request the library has no kernel for (e.g. d = 96 for bf16) */
   ATTN_ERR_MISALIGNED = 3,  /* q/k/v/o not 16-byte aligned (o: 32 for bf16/e4m3), lse not 4-byte */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; see attn_last_error()            */
   ATTN_ERR_TIMEOUT = 5      /* a device-side wait exceeded its limit (attn_get_device_status)      */
