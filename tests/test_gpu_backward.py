@@ -128,3 +128,25 @@ def test_long_causal_backward_is_the_same_in_both_grid_orders(monkeypatch):
     b = _grads(1, 8, 32768, 128, True, seed=41)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert float((a[0] - b[0]).abs().max()) <= 1e-3 * max(1.0, float(a[0].abs().max()))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_outputs_outside_the_valid_rows_are_untouched(d, causal):
+    """Rows past N of dq, dk and dv are never written (at d = 128 dV and dK leave
+    through TMA stores that the tensor map clips at N): a guard band after each
+    output keeps its sentinel, and dK, dV equal those of a call without it."""
+    N = 300
+    q, k, v = inputs.make_qkv_f32(1, 1, N, d, seed=9)
+    do = inputs.make_dout_f32(1, 1, N, d, seed=10)
+    dev = [inputs.to_bf16(t).cuda() for t in (q, k, v, do)]
+    o, lse = binding.attn_fwd(dev[0], dev[1], dev[2], causal=causal)
+    bigs = [torch.full((1, 1, N + 64, d), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    outs = [b[:, :, :N] for b in bigs]
+    binding.attn_bwd(dev[0], dev[1], dev[2], o, lse, dev[3], dq=outs[0], dk=outs[1], dv=outs[2], causal=causal)
+    ref = binding.attn_bwd(dev[0], dev[1], dev[2], o, lse, dev[3], causal=causal)
+    torch.cuda.synchronize()
+    assert binding.get_device_status() == 0
+    for name, big in zip(("dq", "dk", "dv"), bigs):
+        assert bool((big[:, :, N:] == 7.0).all()), name
+    assert torch.equal(outs[1], ref[1]) and torch.equal(outs[2], ref[2])
