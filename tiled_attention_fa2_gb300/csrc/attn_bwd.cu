@@ -24,7 +24,8 @@
 //              TMEM and stage it for the reduce-adds;
 //   warp 8     TMA producer: K_j, V_j once, then Q_i, dO_i and the tile's L and D
 //              vectors into one of two slots, one query tile ahead; it also
-//              issues the dQ reduce-adds from the slots;
+//              issues the dQ reduce-adds from the slots (d = 128: the dO half
+//              of a slot first, so that dO reloads while the Q half is read);
 //   warp 9     MMA issuer, per query tile i:
 //                dV += P^T dO_i, dK += dS^T Q_i   (A from TMEM; half of each once the
 //                                                   first 32-query chunks are written;
@@ -37,7 +38,8 @@
 // producer warp issues the reduce-adds into the fp32 accumulator and waits for
 // them to read the slot before loading the query tile after next into it, so
 // neither the reduce nor its completion sits on the pass warps' path.  After an
-// item's last query tile: dK * scale and dV to bf16.  Across items the next item
+// item's last query tile: dK * scale and dV to bf16 (d = 128: staged per warp in
+// the then idle dS^T buffer and written by TMA stores).  Across items the next item
 // starts under the current one's tail: its first Q, dO load into the slot the
 // finished query tiles freed, its K, V as soon as the last MMA that reads the
 // current ones completes, and its S^T, dP^T while the pass warps drain the last
