@@ -84,18 +84,11 @@ struct TcCfg {
   static constexpr uint32_t kOCol0 = 256;
 };
 
-
 template <int kCols>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kCols]) {
   if constexpr (kCols == 128) tmem_ld128_sync(taddr, r);
   else if constexpr (kCols == 64) tmem_ld64_sync(taddr, r);
   else tmem_ld32_sync(taddr, r);
-}
-template <int kCols>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[kCols]) {
-  if constexpr (kCols == 128) tmem_st128_sync(taddr, r);
-  else if constexpr (kCols == 64) tmem_st64_sync(taddr, r);
-  else tmem_st32_sync(taddr, r);
 }
 
 // A shared-memory descriptor advanced by `off` (bytes / 16) in its start
