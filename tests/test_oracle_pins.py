@@ -176,6 +176,20 @@ def test_causal_first_row_is_v0_and_last_row_is_full():
     np.testing.assert_allclose(lse[:, -1], l_f[:, -1], rtol=0, atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_sequence(causal):
+    """N = 1, the smallest size the library accepts: the one weight is 1, so O is
+    the value row and L is the one score, for the definition and the tiled form."""
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((4, 1, 12)) for _ in range(3))
+    scale = 0.3
+    want_l = scale * (q[:, 0] * k[:, 0]).sum(-1)
+    for o, lse in (oracle.attention_reference(q, k, v, scale, causal),
+                   oracle.attention_tiled(q, k, v, scale, causal, 16, 16)):
+        np.testing.assert_allclose(o[:, 0], v[:, 0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[:, 0], want_l, rtol=0, atol=1e-14)
+
+
 # ---------------------------------------------------------------- invariants
 
 
