@@ -191,6 +191,9 @@ int attn_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o,
  *                      and two fp32 per row, each head's rows padded to a
  *                      multiple of 128), overwritten by every call.
  *   d in {64, 128}; B*H <= 65535.  Other arguments and errors as attn_fwd.
+ *   The outputs and the workspace overlap neither each other nor the inputs:
+ *   the main kernel may start while the preparation kernel still reads o and
+ *   dout (programmatic dependent launch).
  * The launch order of a causal backward (key tile by key tile across heads, or
  * head by head) is chosen from the sizes; the environment variable
  * ATTN_BWD_GRID_ORDER=key or =head, read at each call, forces one.  dk and dv

@@ -44,8 +44,12 @@
 // finished query tiles freed, its K, V as soon as the last MMA that reads the
 // current ones completes, and its S^T, dP^T while the pass warps drain the last
 // dQ and read dV, dK out; only its first dV/dK products wait for that read-out.
+// The main and conversion kernels are launched with programmatic stream
+// serialisation: each starts under its predecessor's tail and waits on the
+// device for that predecessor's results before it reads them.
 #include <cstdlib>
 #include <cstring>
+#include <utility>
 
 #include <cuda_bf16.h>
 
@@ -142,6 +146,14 @@ __device__ __forceinline__ void bulk_wait_read_all_but_last() {
 }
 // Every committed group has completed (its global writes are done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Programmatic dependent launch.  The kernel launched after this one with
+// programmatic stream serialisation may start once every CTA of this grid has
+// executed launch_dependents or exited; all of this grid's CTAs are then
+// resident or done, so the early start cannot take their SMs away.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Returns once the grid this one was launched behind has completed and its
+// memory writes are visible (at once when there is no such grid).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Contiguous global -> shared copy (16-byte aligned addresses, size a multiple
 // of 16), completion counted in bytes on `bar`; elected lane.
@@ -259,6 +271,9 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
 // One warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, int n_pad) {
+  // The main kernel may launch under this grid's last wave: it waits for this
+  // grid's results before it reads them.
+  grid_launch_dependents();
   const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (prow >= static_cast<long long>(p.BH) * n_pad) return;
@@ -296,6 +311,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, i
 
 // dQ (bf16) = the fp32 accumulator, four elements per thread and step.
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, long long n4) {
+  grid_dependency_wait();  // launched behind the main kernel: its reduce-adds are complete
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const float4 v = reinterpret_cast<const float4*>(p.dq_acc)[i];
@@ -468,6 +484,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_tc_kernel(const __gri
 
   if (warp == kProducerWarp) {
     // ============================================================ TMA producer
+    // The kernel may start under the preparation kernel (programmatic launch):
+    // the row vectors and the zeroed dQ accumulator it writes are read and
+    // reduce-added only by this warp, after this wait.
+    grid_dependency_wait();
     // (b*h, query tile) of the last kSl steps, by slot: where their dQ goes.
     int ring_bh[kSl], ring_q[kSl];
     // dQ of step t, staged in its slot by the pass warps: reduce-add the boxes
@@ -850,6 +870,25 @@ cudaError_t causal_head_major(int* out) {
   return cudaSuccess;
 }
 
+// Launches `kern` with programmatic stream serialisation: it may start before
+// the previous kernel in the stream has finished, and waits for that kernel's
+// results on the device (grid_dependency_wait) before it reads them.
+template <class... Params, class... Args>
+cudaError_t launch_behind(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, bool kCausal>
 cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   auto kern = attn_bwd_tc_kernel<D, kCausal>;
@@ -864,8 +903,8 @@ cudaError_t launch_main(const BwdParams& p, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long items = n_kt * p.BH;
   const long long grid = items < sms ? items : sms;  // persistent: at most one CTA per SM
-  kern<<<static_cast<unsigned>(grid), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(p, head_major);
-  return cudaGetLastError();
+  return launch_behind(kern, dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream, p,
+                       head_major);
 }
 
 }  // namespace
@@ -892,8 +931,7 @@ cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stre
   const long long n4 = static_cast<long long>(p.BH) * p.N * d / 4;
   const long long want = (n4 + 255) / 256;
   const unsigned blocks = static_cast<unsigned>(want < 152LL * 16 ? want : 152LL * 16);
-  attn_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(p, n4);
-  return cudaGetLastError();
+  return launch_behind(attn_bwd_dq_kernel, dim3(blocks), dim3(256), 0, stream, p, n4);
 }
 
 }  // namespace attn
