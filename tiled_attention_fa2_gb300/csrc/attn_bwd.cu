@@ -268,44 +268,64 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
 // Per row of every head, padded to whole 128-row tiles: -L log2 e (-inf on
 // padding rows, so their P is 0) and -D with D = sum_c dO_c O_c (0 on padding
 // rows), negated so the pass adds them; real rows of the dQ accumulator zeroed.
-// One warp per row.
+// A row is read by d/8 lanes, 16 bytes of O and of dO each; a warp covers
+// 256/d rows per access and kPrepIter accesses, all issued before the first
+// product so that each lane keeps several loads in flight.
+constexpr int kPrepIter = 4;
+template <int D>
+constexpr int prep_rows_per_block() {
+  return 8 /*warps*/ * (32 / (D / 8)) * kPrepIter;
+}
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, int n_pad) {
   // The main kernel may launch under this grid's last wave: it waits for this
   // grid's results before it reads them.
   grid_launch_dependents();
-  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (prow >= static_cast<long long>(p.BH) * n_pad) return;
-  const int bh = static_cast<int>(prow / n_pad), r = static_cast<int>(prow % n_pad);
-  if (r >= p.N) {
-    if (lane == 0) {
-      p.lse2[prow] = -INFINITY;
-      p.drow[prow] = 0.f;
+  constexpr int kLanes = D / 8;         // lanes per row: 16 bytes of bf16 each
+  constexpr int kRows = 32 / kLanes;    // rows per warp access
+  const int lane = threadIdx.x & 31, sub = lane / kLanes, piece = lane % kLanes;
+  const long long total = static_cast<long long>(p.BH) * n_pad;
+  const long long row0 =
+      (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * (kRows * kPrepIter) + sub;
+  uint4 ov[kPrepIter], gv[kPrepIter];
+  long long row[kPrepIter];  // row of O, dO, L and the accumulator; -1: padding or past the end
+#pragma unroll
+  for (int k = 0; k < kPrepIter; ++k) {
+    const long long prow = row0 + k * kRows;
+    row[k] = -1;
+    ov[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (prow < total) {
+      const int bh = static_cast<int>(prow / n_pad), r = static_cast<int>(prow % n_pad);
+      if (r < p.N) {
+        row[k] = static_cast<long long>(bh) * p.N + r;
+        ov[k] = reinterpret_cast<const uint4*>(p.o)[row[k] * kLanes + piece];
+        gv[k] = reinterpret_cast<const uint4*>(p.dout)[row[k] * kLanes + piece];
+      }
     }
-    return;
-  }
-  const long long row = static_cast<long long>(bh) * p.N + r;
-  // d / 32 elements per lane, moved with one vector access each.
-  float acc = 0.f;
-  if constexpr (D == 128) {
-    const uint2 ov = reinterpret_cast<const uint2*>(p.o)[row * 32 + lane];
-    const uint2 gv = reinterpret_cast<const uint2*>(p.dout)[row * 32 + lane];
-    const float2 o0 = bf16x2_to_f2(ov.x), o1 = bf16x2_to_f2(ov.y), g0 = bf16x2_to_f2(gv.x), g1 = bf16x2_to_f2(gv.y);
-    acc = fmaf(o0.x, g0.x, fmaf(o0.y, g0.y, fmaf(o1.x, g1.x, o1.y * g1.y)));
-    reinterpret_cast<float4*>(p.dq_acc)[row * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    const uint32_t ov = reinterpret_cast<const uint32_t*>(p.o)[row * 32 + lane];
-    const uint32_t gv = reinterpret_cast<const uint32_t*>(p.dout)[row * 32 + lane];
-    const float2 o0 = bf16x2_to_f2(ov), g0 = bf16x2_to_f2(gv);
-    acc = fmaf(o0.x, g0.x, o0.y * g0.y);
-    reinterpret_cast<float2*>(p.dq_acc)[row * 32 + lane] = make_float2(0.f, 0.f);
   }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    p.drow[prow] = -acc;
-    p.lse2[prow] = -p.lse[row] * 1.4426950408889634f;
+  for (int k = 0; k < kPrepIter; ++k) {
+    const long long prow = row0 + k * kRows;
+    float acc = 0.f;
+    if (row[k] >= 0) {
+      const uint32_t o4[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w}, g4[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float2 o2 = bf16x2_to_f2(o4[c]), g2 = bf16x2_to_f2(g4[c]);
+        acc = fmaf(o2.x, g2.x, fmaf(o2.y, g2.y, acc));
+      }
+      // d fp32 per accumulator row: two 16-byte pieces per lane.
+      float4* dq = reinterpret_cast<float4*>(p.dq_acc) + row[k] * (D / 4) + 2 * piece;
+      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // Sum over the row's lanes (every lane takes part; padding rows add zeros).
+#pragma unroll
+    for (int m = kLanes / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (piece == 0 && prow < total) {
+      p.drow[prow] = row[k] >= 0 ? -acc : 0.f;
+      p.lse2[prow] = row[k] >= 0 ? -p.lse[row[k]] * 1.4426950408889634f : -INFINITY;
+    }
   }
 }
 
@@ -920,9 +940,13 @@ cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stre
   if (d != 64 && d != 128) return cudaErrorInvalidValue;
   const int n_pad = (p.N + 127) / 128 * 128;
   const long long prows = static_cast<long long>(p.BH) * n_pad;
-  const unsigned prep_blocks = static_cast<unsigned>((prows + 7) / 8);
-  if (d == 128) attn_bwd_prep_kernel<128><<<prep_blocks, 256, 0, stream>>>(p, n_pad);
-  else attn_bwd_prep_kernel<64><<<prep_blocks, 256, 0, stream>>>(p, n_pad);
+  if (d == 128) {
+    constexpr int rpb = prep_rows_per_block<128>();
+    attn_bwd_prep_kernel<128><<<static_cast<unsigned>((prows + rpb - 1) / rpb), 256, 0, stream>>>(p, n_pad);
+  } else {
+    constexpr int rpb = prep_rows_per_block<64>();
+    attn_bwd_prep_kernel<64><<<static_cast<unsigned>((prows + rpb - 1) / rpb), 256, 0, stream>>>(p, n_pad);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (d == 128) e = causal ? launch_main<128, true>(p, stream) : launch_main<128, false>(p, stream);
