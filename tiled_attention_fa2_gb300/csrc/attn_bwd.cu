@@ -329,16 +329,24 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p, i
   }
 }
 
-// dQ (bf16) = the fp32 accumulator, four elements per thread and step.
+// dQ (bf16) = the fp32 accumulator.  A block converts 4 x 256 consecutive
+// groups of four elements per pass, each thread four groups 256 apart, all four
+// loads issued before the first store.
+constexpr int kDqPerThread = 4;
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p, long long n4) {
   grid_dependency_wait();  // launched behind the main kernel: its reduce-adds are complete
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(p.dq_acc)[i];
-    uint2 out;
-    out.x = pack_bf16x2(v.x, v.y);
-    out.y = pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint2*>(p.dq)[i] = out;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc);
+  uint2* dst = reinterpret_cast<uint2*>(p.dq);
+  const long long per_pass = static_cast<long long>(gridDim.x) * 256 * kDqPerThread;
+  for (long long base = static_cast<long long>(blockIdx.x) * 256 * kDqPerThread + threadIdx.x; base < n4;
+       base += per_pass) {
+    float4 v[kDqPerThread];
+#pragma unroll
+    for (int k = 0; k < kDqPerThread; ++k)
+      if (base + 256 * k < n4) v[k] = src[base + 256 * k];
+#pragma unroll
+    for (int k = 0; k < kDqPerThread; ++k)
+      if (base + 256 * k < n4) dst[base + 256 * k] = make_uint2(pack_bf16x2(v[k].x, v[k].y), pack_bf16x2(v[k].z, v[k].w));
   }
 }
 
@@ -953,7 +961,7 @@ cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, cudaStream_t stre
   else e = causal ? launch_main<64, true>(p, stream) : launch_main<64, false>(p, stream);
   if (e != cudaSuccess) return e;
   const long long n4 = static_cast<long long>(p.BH) * p.N * d / 4;
-  const long long want = (n4 + 255) / 256;
+  const long long want = (n4 + 256 * kDqPerThread - 1) / (256 * kDqPerThread);
   const unsigned blocks = static_cast<unsigned>(want < 152LL * 16 ? want : 152LL * 16);
   return launch_behind(attn_bwd_dq_kernel, dim3(blocks), dim3(256), 0, stream, p, n4);
 }
