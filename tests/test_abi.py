@@ -157,6 +157,8 @@ def call_bwd(lib, **kw):
     (dict(q=None), 1), (dict(dout=None), 1), (dict(dv=None), 1), (dict(ws=None), 1), (dict(N=0), 1),
     (dict(causal=3), 1), (dict(scale=0.0), 1), (dict(wsb=1024), 1), (dict(d=96), 2), (dict(d=32), 2),
     (dict(dq=FAKE + 8), 3), (dict(dout=FAKE + 4), 3), (dict(ws=FAKE + 16), 3), (dict(B=300, H=300, N=8), 2),
+    # the preparation kernel reads o and dout 16 bytes at a time
+    (dict(o=FAKE + 8), 3), (dict(dout=FAKE + 8), 3),
 ])
 def test_backward_entry_rejects_bad_arguments_on_the_host(lib, kw, status):
     assert call_bwd(lib, **kw) == status
